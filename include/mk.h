@@ -1,0 +1,175 @@
+/* mk.h -- C ABI of libmk.so, a single-GPU batch-1 decode engine for Qwen3-0.6B-shaped
+ * transformers on NVIDIA GB300 (sm_103a).
+ *
+ * One call of mk_decode_step runs ONE persistent kernel that executes every layer and the
+ * LM-head argmax, so one launch produces one token ("One kernel per token", monolith page,
+ * "Why it's exciting"; "fold the LM head and argmax into the megakernel", monolith page,
+ * "Design decisions", sync experiment 5).
+ *
+ * Conventions for every entry point below:
+ *  - Pointers named *_dev are device pointers; the caller allocates and owns them and keeps them
+ *    alive for as long as the library may read or write them. Pointers named *_host are host
+ *    pointers. `stream` is a cudaStream_t passed as void* (NULL = the legacy default stream).
+ *  - Calls return MK_OK (0) or a negative MK_E* code; they never abort the process.
+ *  - No entry point allocates device memory except where stated; the model's workspace is a
+ *    caller-owned device buffer of mk_workspace_bytes() bytes.
+ *  - All weight matrices are row-major with rows = output features, cols = input features
+ *    ("canonical packed form"); see mk_mat.
+ */
+#ifndef MK_H
+#define MK_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- status codes */
+#define MK_OK 0
+#define MK_EINVAL (-1)       /* bad shape, format, alignment, token or position */
+#define MK_ECUDA (-2)        /* a CUDA runtime call failed (text in mk_last_error) */
+#define MK_ETIMEOUT (-3)     /* a device-side wait exceeded its deadline; the step was abandoned */
+#define MK_ENORESIDENT (-4)  /* the persistent grid cannot be made co-resident on this GPU */
+#define MK_ENOTRACE (-5)     /* X-ray requested but the model was created without it */
+
+/* ---------------------------------------------------------------- weight formats
+ * MK_BF16:    data = bf16 [rows][cols]; scale = NULL.
+ * MK_FP8_ROW: data = OCP FP8 E4M3 bytes [rows][cols]; scale = fp32 [rows], one per output row;
+ *             w = e4m3(code) * scale[row]  ("FP8 format", monolith page, "Design decisions").
+ * MK_NVFP4:   data = E2M1 codes [rows][cols/2], element 2j in the low nibble of byte j;
+ *             scale = E4M3 bytes [rows][cols/16], one per 16 consecutive inputs of a row;
+ *             tensor_scale = fp32; w = e2m1(code) * e4m3(block scale) * tensor_scale
+ *             ("NVFP4 format", monolith page, "Design decisions"; E2M1 grid: TSCT super-kernel
+ *             page, section 3b).
+ * Every data/scale pointer must be 16-byte aligned. */
+enum mk_fmt { MK_BF16 = 0, MK_FP8_ROW = 1, MK_NVFP4 = 2 };
+
+typedef struct {
+  const void* data;   /* device */
+  const void* scale;  /* device or NULL (bf16) */
+  float tensor_scale; /* NVFP4 only */
+  int fmt;            /* enum mk_fmt */
+} mk_mat;
+
+/* Model shape. This build supports the Qwen3-0.6B shape family: hidden 1024, 16 query heads,
+ * 8 KV heads of width 128, FFN 3072 (model bullet, monolith page, "Upstream facts"); any
+ * 1 <= n_layers <= 64, 1 <= vocab < 2^24, 1 <= max_ctx <= mk_max_context(). */
+typedef struct {
+  int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_ctx;
+  float rope_theta; /* 1e6 for Qwen3 */
+  float rms_eps;    /* 1e-6 for Qwen3 */
+} mk_config;
+
+/* One decoder layer. q/k/v must share one format, and gate/up must share one format.
+ * Norm weights are bf16 device vectors: ln_in/ln_post [hidden], q_norm/k_norm [head_dim]. */
+typedef struct {
+  mk_mat q, k, v, o, gate, up, down;
+  const void *ln_in, *ln_post, *q_norm, *k_norm;
+} mk_layer;
+
+/* The tied embedding / LM-head matrix [vocab][hidden] is MK_BF16 or MK_FP8_ROW (the LM head
+ * stays FP8 in the NVFP4 variant: "The LM head stays FP8", monolith page, NVFP4 format). */
+typedef struct {
+  const mk_layer* layers; /* host array of n_layers entries (copied by mk_create) */
+  mk_mat embed;
+  const void* final_norm; /* bf16 [hidden], device */
+} mk_weights;
+
+typedef struct mk_model mk_model; /* opaque; library-owned host object */
+
+/* mk_create flags */
+#define MK_FLAG_XRAY 1u /* keep per-CTA per-phase timestamps of the last step (mk_trace_dump) */
+
+/* ---------------------------------------------------------------- model lifetime */
+
+/* Largest max_ctx this build accepts on the current device (attention splits the context into
+ * at most one unit per SM, each holding up to 320 positions in shared memory). */
+int mk_max_context(void);
+
+/* Bytes of device workspace a model needs: bf16 KV cache [n_layers][n_kv][max_ctx][head_dim] for
+ * keys and for values, a RoPE cos/sin table, activations, sync counters, an optional per-layer
+ * hidden-state buffer and, with MK_FLAG_XRAY, the trace buffer. Returns 0 on a bad config. */
+size_t mk_workspace_bytes(const mk_config* cfg, unsigned flags);
+
+/* Validate the config and weights, lay out the caller's zeroed-or-not workspace (it is cleared
+ * here), upload the layer table and build the RoPE table, all on `stream`. The weights and the
+ * workspace must outlive the model. On success *out receives the handle. */
+int mk_create(const mk_config* cfg, const mk_weights* w, void* workspace_dev, size_t workspace_bytes,
+              void* stream, unsigned flags, mk_model** out);
+
+void mk_destroy(mk_model* m);
+
+/* Text of the last error on this model (or of the last mk_create failure when m == NULL). */
+const char* mk_last_error(const mk_model* m);
+
+/* ---------------------------------------------------------------- decoding */
+
+/* One decode step: embed `token`, write its K/V at position `pos`, attend over 0..pos in every
+ * layer, and return the argmax of the logits (lowest index among equal maxima) in
+ * *next_token_host. If logits_dev != NULL, the fp32 logits [vocab] are written there.
+ * Positions < pos must already be filled (by earlier steps or through mk_kv_cache).
+ * Synchronises `stream` once at the end. Deterministic for identical inputs. */
+int mk_decode_step(mk_model* m, int32_t token, int32_t pos, int32_t* next_token_host, float* logits_dev);
+
+/* n greedy steps without host round trips: step i (0-based) runs at position pos0 + i on the
+ * token produced by step i-1 (step 0 on first_token); every launch reads its input token from
+ * device memory. tokens_dev (device int32 [n]) receives the produced tokens. Does not
+ * synchronise; errors of the device steps are reported by the next mk_sync. */
+int mk_decode_greedy(mk_model* m, int32_t first_token, int32_t pos0, int32_t n, int32_t* tokens_dev);
+
+/* Wait for the model's stream and report any device-side status (e.g. MK_ETIMEOUT). */
+int mk_sync(mk_model* m);
+
+/* Device pointers to layer `layer`'s bf16 K and V caches, each [n_kv_heads][max_ctx][head_dim],
+ * for prefilling or inspecting the cache. */
+int mk_kv_cache(mk_model* m, int layer, void** k_dev, void** v_dev);
+
+/* Copy the residual stream of the last step into out_dev (device fp32 [(n_layers+1)][hidden]):
+ * row 0 = embedding output, row l+1 = residual after layer l. */
+int mk_debug_hidden(mk_model* m, float* out_dev);
+
+/* X-ray: copy the last step's trace (24-byte records: u64 globaltimer, u64 clock64, u32 smid,
+ * u16 cta, u8 phase, u8 kind) into host_buf. Returns MK_ENOTRACE without MK_FLAG_XRAY. */
+int mk_trace_dump(mk_model* m, void* host_buf, size_t cap, size_t* written);
+
+/* Test hook: make CTA `cta` skip its signal after phase `phase` of layer 0 in the next steps, so
+ * that every wait on it runs out; with timeout_ms the device deadline of every wait. Pass
+ * cta = -1 to disable. The failed step returns MK_ETIMEOUT and the model stays usable. */
+int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms);
+
+/* ---------------------------------------------------------------- building blocks */
+
+/* Quantise a bf16 matrix [rows][cols] into MK_FP8_ROW on the device: scale[r] = fp32(absmax/448),
+ * code = E4M3 round-to-nearest-even, saturating, of fp32(w / scale[r]); an all-zero row gives
+ * scale 0 and zero codes. codes_dev: [rows][cols] bytes; scales_dev: fp32 [rows]. */
+int mk_pack_fp8_row(const void* w_bf16_dev, int rows, int cols, void* codes_dev, float* scales_dev, void* stream);
+
+/* Quantise a bf16 matrix into MK_NVFP4 on the device (cols a multiple of 16):
+ * t = fp32(amax/2688); block scale b = E4M3_RNE(fp32(amax_block / fp32(6 t))); code =
+ * E2M1_RNE_satfinite(fp32(w / fp32(e4m3(b) * t))). tscale_dev (device fp32) receives t; it is
+ * also used as the amax accumulator while the call runs. */
+int mk_pack_nvfp4(const void* w_bf16_dev, int rows, int cols, void* codes_dev, void* bscales_dev,
+                  float* tscale_dev, void* stream);
+
+/* y = W x with the same streaming dequant-GEMV the megakernel uses, as one persistent launch.
+ * x_dev: fp32 [cols]; y_dev: fp32 [rows]; cols a multiple of 1024 and at most 4096. */
+int mk_gemv(const mk_mat* w, int rows, int cols, const float* x_dev, float* y_dev, void* stream);
+
+/* Streaming-read probe: read `bytes` (multiple of 16 * 1024 * number of SMs) from buf_dev once
+ * with bulk copies into shared memory, on `stream`. Used to measure achievable HBM bandwidth. */
+int mk_stream_read(const void* buf_dev, size_t bytes, void* stream);
+
+/* Run the hardware conversions on every input, for checking them against a CPU table:
+ * f16_from_e4m3 [65536] = cvt.rn.f16x2.e4m3x2 of every 16-bit pair; f16_from_e2m1 [256] =
+ * cvt.rn.f16x2.e2m1x2 of every byte; e4m3_from_f32 [n/2] and e2m1_from_f32 [n/2] = the
+ * saturating encoders applied to pairs (in[2i], in[2i+1]) of in_dev [n]. All device buffers;
+ * any output may be NULL. */
+int mk_probe_cvt(uint32_t* f16_from_e4m3_dev, uint32_t* f16_from_e2m1_dev, const float* in_dev, int n,
+                 uint16_t* e4m3_from_f32_dev, uint8_t* e2m1_from_f32_dev, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MK_H */

@@ -1,0 +1,408 @@
+// Host implementation of the C ABI declared in include/mk.h.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+
+using namespace mk;
+
+struct mk_model {
+  mk_config cfg;
+  unsigned flags;
+  cudaStream_t stream;
+  int grid;
+  int max_units;
+  // workspace carve-up (device)
+  SyncBlock* sync;
+  DLayer* dlayers;
+  float *h_mlp, *h_attn, *qkv, *att, *act, *attp;
+  float *rope_cos, *rope_sin;
+  uint16_t *kc, *vc;
+  float* hidden_dbg;
+  TraceRec* trace;
+  DMat embed;
+  const uint16_t* final_norm;
+  // host
+  uint32_t* host_status;  // pinned: SyncBlock::status and ::tok lines (64 words)
+  unsigned long long timeout_ns;
+  int fault_cta, fault_phase;
+  std::string err;
+};
+
+static thread_local std::string g_create_err;
+
+static int set_err(mk_model* m, int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (m) m->err = buf;
+  else g_create_err = buf;
+  return code;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct Layout {
+  size_t sync, layers, h_mlp, h_attn, qkv, att, act, attp, rope_cos, rope_sin, kc, vc, hidden, trace, total;
+};
+
+static int device_grid(int* grid) {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  *grid = sms;
+  return 0;
+}
+
+static int max_units_for(int grid) {
+  int u = grid / NKVH;
+  return u > MAXC ? MAXC : u;
+}
+
+static bool layout_of(const mk_config* c, unsigned flags, int grid, Layout* L) {
+  if (!c || c->n_layers < 1 || c->max_ctx < 1 || c->vocab < 1) return false;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256);
+    return at;
+  };
+  const size_t kv = (size_t)c->n_layers * NKVH * c->max_ctx * HD * sizeof(uint16_t);
+  L->sync = take(sizeof(SyncBlock));
+  L->layers = take(sizeof(DLayer) * c->n_layers);
+  L->h_mlp = take(HID * 4);
+  L->h_attn = take(HID * 4);
+  L->qkv = take(QKV_ROWS * 4);
+  L->att = take(QROWS * 4);
+  L->act = take(FFN * 4);
+  L->attp = take((size_t)NKVH * MAXC * 2 * PART_STRIDE * 4);
+  L->rope_cos = take((size_t)c->max_ctx * (HD / 2) * 4);
+  L->rope_sin = take((size_t)c->max_ctx * (HD / 2) * 4);
+  L->hidden = take((size_t)(c->n_layers + 1) * HID * 4);
+  L->trace = take((flags & MK_FLAG_XRAY) ? (size_t)grid * TRACE_PER_CTA * sizeof(TraceRec) : 0);
+  L->kc = take(kv);
+  L->vc = take(kv);
+  L->total = o;
+  return true;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int check_mat(const mk_mat& m, int rows, int cols, const char* name, bool allow_nvfp4) {
+  if (m.fmt < MK_BF16 || m.fmt > MK_NVFP4) return set_err(nullptr, MK_EINVAL, "%s: bad format %d", name, m.fmt);
+  if (m.fmt == MK_NVFP4 && !allow_nvfp4) return set_err(nullptr, MK_EINVAL, "%s: NVFP4 not allowed here", name);
+  if (!m.data || !aligned16(m.data)) return set_err(nullptr, MK_EINVAL, "%s: data NULL or not 16-byte aligned", name);
+  if (m.fmt != MK_BF16 && (!m.scale || !aligned16(m.scale)))
+    return set_err(nullptr, MK_EINVAL, "%s: scale NULL or not 16-byte aligned", name);
+  if (cols % 1024 != 0 || rows < 1) return set_err(nullptr, MK_EINVAL, "%s: unsupported shape", name);
+  return MK_OK;
+}
+
+static DMat to_dmat(const mk_mat& m) {
+  DMat d;
+  d.data = (const uint8_t*)m.data;
+  d.scale = (const uint8_t*)m.scale;
+  d.tscale = m.tensor_scale;
+  d.fmt = m.fmt;
+  return d;
+}
+
+extern "C" {
+
+int mk_max_context(void) {
+  int grid;
+  if (device_grid(&grid)) return 0;
+  return max_units_for(grid) * UNIT_POS;
+}
+
+size_t mk_workspace_bytes(const mk_config* cfg, unsigned flags) {
+  int grid;
+  if (device_grid(&grid)) return 0;
+  Layout L = {};
+  if (!layout_of(cfg, flags, grid, &L)) return 0;
+  return L.total;
+}
+
+const char* mk_last_error(const mk_model* m) { return m ? m->err.c_str() : g_create_err.c_str(); }
+
+int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes, void* stream, unsigned flags,
+              mk_model** out) {
+  if (!out) return set_err(nullptr, MK_EINVAL, "out is NULL");
+  *out = nullptr;
+  if (!c || !w || !w->layers) return set_err(nullptr, MK_EINVAL, "config or weights NULL");
+  if (c->hidden != HID || c->n_q_heads != NQH || c->n_kv_heads != NKVH || c->head_dim != HD || c->ffn != FFN)
+    return set_err(nullptr, MK_EINVAL, "only the Qwen3-0.6B shape family (1024/16/8/128/3072) is supported");
+  if (c->n_layers < 1 || c->n_layers > 64 || c->vocab < 1 || c->vocab >= (1 << 24) || c->max_ctx < 1)
+    return set_err(nullptr, MK_EINVAL, "bad n_layers/vocab/max_ctx");
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return set_err(nullptr, MK_EINVAL, "bad eps/theta");
+  int grid;
+  if (device_grid(&grid)) return set_err(nullptr, MK_ECUDA, "cannot query the device");
+  if (grid < 64) return set_err(nullptr, MK_ENORESIDENT, "need at least 64 SMs, device has %d", grid);
+  const int max_units = max_units_for(grid);
+  if (c->max_ctx > max_units * UNIT_POS)
+    return set_err(nullptr, MK_EINVAL, "max_ctx %d exceeds %d on this device", c->max_ctx, max_units * UNIT_POS);
+  int dev = 0, coop = 0, bps = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (!coop) return set_err(nullptr, MK_ENORESIDENT, "device lacks cooperative launch");
+  if (decode_occupancy(&bps) || bps < 1)
+    return set_err(nullptr, MK_ENORESIDENT, "persistent CTA (%d threads, %d B smem) does not fit an SM", NTHREADS,
+                   decode_smem_bytes());
+  Layout L = {};
+  layout_of(c, flags, grid, &L);
+  if (!ws || ws_bytes < L.total || !aligned16(ws))
+    return set_err(nullptr, MK_EINVAL, "workspace too small or unaligned (%zu < %zu)", ws_bytes, L.total);
+  // weights
+  int rc;
+  std::vector<DLayer> dl(c->n_layers);
+  for (int l = 0; l < c->n_layers; ++l) {
+    const mk_layer& ly = w->layers[l];
+    const mk_mat* mats[7] = {&ly.q, &ly.k, &ly.v, &ly.o, &ly.gate, &ly.up, &ly.down};
+    const int rws[7] = {QROWS, KVROWS, KVROWS, HID, FFN, FFN, HID};
+    const int cls[7] = {HID, HID, HID, QROWS, HID, HID, FFN};
+    const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
+    for (int i = 0; i < 7; ++i) {
+      if ((rc = check_mat(*mats[i], rws[i], cls[i], names[i], true)) != MK_OK) return rc;
+      dl[l].m[i] = to_dmat(*mats[i]);
+    }
+    if (ly.q.fmt != ly.k.fmt || ly.q.fmt != ly.v.fmt)
+      return set_err(nullptr, MK_EINVAL, "layer %d: q, k, v must share one format", l);
+    if (ly.gate.fmt != ly.up.fmt) return set_err(nullptr, MK_EINVAL, "layer %d: gate and up must share one format", l);
+    if (!ly.ln_in || !ly.ln_post || !ly.q_norm || !ly.k_norm)
+      return set_err(nullptr, MK_EINVAL, "layer %d: norm weight NULL", l);
+    dl[l].ln_in = (const uint16_t*)ly.ln_in;
+    dl[l].ln_post = (const uint16_t*)ly.ln_post;
+    dl[l].q_norm = (const uint16_t*)ly.q_norm;
+    dl[l].k_norm = (const uint16_t*)ly.k_norm;
+  }
+  if ((rc = check_mat(w->embed, c->vocab, HID, "embed", false)) != MK_OK) return rc;
+  if (!w->final_norm) return set_err(nullptr, MK_EINVAL, "final_norm NULL");
+
+  mk_model* m = new mk_model();
+  m->cfg = *c;
+  m->flags = flags;
+  m->stream = (cudaStream_t)stream;
+  m->grid = grid;
+  m->max_units = max_units;
+  uint8_t* base = (uint8_t*)ws;
+  m->sync = (SyncBlock*)(base + L.sync);
+  m->dlayers = (DLayer*)(base + L.layers);
+  m->h_mlp = (float*)(base + L.h_mlp);
+  m->h_attn = (float*)(base + L.h_attn);
+  m->qkv = (float*)(base + L.qkv);
+  m->att = (float*)(base + L.att);
+  m->act = (float*)(base + L.act);
+  m->attp = (float*)(base + L.attp);
+  m->rope_cos = (float*)(base + L.rope_cos);
+  m->rope_sin = (float*)(base + L.rope_sin);
+  m->kc = (uint16_t*)(base + L.kc);
+  m->vc = (uint16_t*)(base + L.vc);
+  m->hidden_dbg = (float*)(base + L.hidden);
+  m->trace = (flags & MK_FLAG_XRAY) ? (TraceRec*)(base + L.trace) : nullptr;
+  m->embed = to_dmat(w->embed);
+  m->final_norm = (const uint16_t*)w->final_norm;
+  m->timeout_ns = 500000000ull;
+  m->fault_cta = -1;
+  m->fault_phase = -1;
+  if (cudaMallocHost(&m->host_status, 64 * sizeof(uint32_t)) != cudaSuccess) {
+    delete m;
+    return set_err(nullptr, MK_ECUDA, "cudaMallocHost failed");
+  }
+  cudaError_t e = cudaMemsetAsync(ws, 0, L.total, m->stream);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(m->dlayers, dl.data(), sizeof(DLayer) * c->n_layers, cudaMemcpyHostToDevice, m->stream);
+  if (e == cudaSuccess && launch_rope_table(m->rope_cos, m->rope_sin, c->max_ctx, c->rope_theta, m->stream))
+    e = cudaGetLastError();
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) {
+    set_err(nullptr, MK_ECUDA, "mk_create: %s", cudaGetErrorString(e));
+    cudaFreeHost(m->host_status);
+    delete m;
+    return MK_ECUDA;
+  }
+  *out = m;
+  return MK_OK;
+}
+
+void mk_destroy(mk_model* m) {
+  if (!m) return;
+  if (m->host_status) cudaFreeHost(m->host_status);
+  delete m;
+}
+
+static int units_for(const mk_model* m, int pos) {
+  int u = (pos + 1 + KVT - 1) / KVT;
+  if (u > m->max_units) u = m->max_units;
+  if (u < 1) u = 1;
+  return u;
+}
+
+static KParams base_params(mk_model* m) {
+  KParams p = {};
+  p.layers = m->dlayers;
+  p.n_layers = m->cfg.n_layers;
+  p.embed = m->embed;
+  p.final_norm = m->final_norm;
+  p.vocab = m->cfg.vocab;
+  p.max_ctx = m->cfg.max_ctx;
+  p.eps = m->cfg.rms_eps;
+  p.kc = m->kc;
+  p.vc = m->vc;
+  p.rope_cos = m->rope_cos;
+  p.rope_sin = m->rope_sin;
+  p.h_mlp = m->h_mlp;
+  p.h_attn = m->h_attn;
+  p.qkv = m->qkv;
+  p.att = m->att;
+  p.act = m->act;
+  p.attp = m->attp;
+  p.sync = m->sync;
+  p.hidden_dbg = m->hidden_dbg;
+  p.trace = m->trace;
+  p.timeout_ns = m->timeout_ns;
+  p.fault_cta = m->fault_cta;
+  p.fault_phase = m->fault_phase;
+  return p;
+}
+
+// Read the device status; on a failed step clear the sync block so the model stays usable.
+static int collect_status(mk_model* m, int32_t* next_token) {
+  cudaError_t e = cudaMemcpyAsync(m->host_status, m->sync->status, 64 * sizeof(uint32_t), cudaMemcpyDeviceToHost,
+                                  m->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) return set_err(m, MK_ECUDA, "decode: %s", cudaGetErrorString(e));
+  const uint32_t st = m->host_status[0];
+  if (st == 4) {
+    set_err(m, MK_EINVAL, "a device step read an out-of-range input token");
+    cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
+    cudaStreamSynchronize(m->stream);
+    return MK_EINVAL;
+  }
+  if (st != 0) {
+    const uint32_t d = m->host_status[1];
+    set_err(m, MK_ETIMEOUT, "device wait timed out: phase %u layer %u cta %u%s", d & 0xFF, (d >> 8) & 0xFF,
+            (d >> 16) & 0x7FFF, (d & 0x80000000u) ? " (weight stream)" : "");
+    cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
+    cudaStreamSynchronize(m->stream);
+    return MK_ETIMEOUT;
+  }
+  if (next_token) *next_token = (int32_t)m->host_status[32];
+  return MK_OK;
+}
+
+int mk_decode_step(mk_model* m, int32_t token, int32_t pos, int32_t* next_token_host, float* logits_dev) {
+  if (!m) return MK_EINVAL;
+  if (token < 0 || token >= m->cfg.vocab) return set_err(m, MK_EINVAL, "token %d out of range", token);
+  if (pos < 0 || pos >= m->cfg.max_ctx) return set_err(m, MK_EINVAL, "pos %d out of range", pos);
+  KParams p = base_params(m);
+  p.token = token;
+  p.token_ptr = nullptr;
+  p.pos = pos;
+  p.next_out = nullptr;
+  p.logits = logits_dev;
+  p.units = units_for(m, pos);
+  if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
+    return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
+  return collect_status(m, next_token_host);
+}
+
+int mk_decode_greedy(mk_model* m, int32_t first_token, int32_t pos0, int32_t n, int32_t* tokens_dev) {
+  if (!m || n < 0 || !tokens_dev) return MK_EINVAL;
+  if (first_token < 0 || first_token >= m->cfg.vocab) return set_err(m, MK_EINVAL, "token out of range");
+  if (pos0 < 0 || (long long)pos0 + n > m->cfg.max_ctx) return set_err(m, MK_EINVAL, "positions out of range");
+  KParams p = base_params(m);
+  for (int i = 0; i < n; ++i) {
+    p.token = first_token;
+    p.token_ptr = i == 0 ? nullptr : tokens_dev + (i - 1);
+    p.pos = pos0 + i;
+    p.next_out = tokens_dev + i;
+    p.logits = nullptr;
+    p.units = units_for(m, p.pos);
+    if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
+      return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
+  }
+  return MK_OK;
+}
+
+int mk_sync(mk_model* m) {
+  if (!m) return MK_EINVAL;
+  return collect_status(m, nullptr);
+}
+
+int mk_kv_cache(mk_model* m, int layer, void** k, void** v) {
+  if (!m || layer < 0 || layer >= m->cfg.n_layers) return MK_EINVAL;
+  const size_t off = (size_t)layer * NKVH * m->cfg.max_ctx * HD;
+  if (k) *k = m->kc + off;
+  if (v) *v = m->vc + off;
+  return MK_OK;
+}
+
+int mk_debug_hidden(mk_model* m, float* out) {
+  if (!m || !out) return MK_EINVAL;
+  cudaError_t e = cudaMemcpyAsync(out, m->hidden_dbg, (size_t)(m->cfg.n_layers + 1) * HID * 4,
+                                  cudaMemcpyDeviceToDevice, m->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  return e == cudaSuccess ? MK_OK : set_err(m, MK_ECUDA, "%s", cudaGetErrorString(e));
+}
+
+int mk_trace_dump(mk_model* m, void* host_buf, size_t cap, size_t* written) {
+  if (!m) return MK_EINVAL;
+  if (!m->trace) return set_err(m, MK_ENOTRACE, "model created without MK_FLAG_XRAY");
+  const size_t bytes = (size_t)m->grid * TRACE_PER_CTA * sizeof(TraceRec);
+  if (!host_buf || cap < bytes) return set_err(m, MK_EINVAL, "trace buffer needs %zu bytes", bytes);
+  cudaError_t e = cudaMemcpyAsync(host_buf, m->trace, bytes, cudaMemcpyDeviceToHost, m->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) return set_err(m, MK_ECUDA, "%s", cudaGetErrorString(e));
+  if (written) *written = bytes;
+  return MK_OK;
+}
+
+int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms) {
+  if (!m) return MK_EINVAL;
+  m->fault_cta = cta;
+  m->fault_phase = phase;
+  if (timeout_ms > 0) m->timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
+  return MK_OK;
+}
+
+int mk_pack_fp8_row(const void* w, int rows, int cols, void* codes, float* scales, void* stream) {
+  if (!w || !codes || !scales || rows < 1 || cols < 2 || cols % 2) return MK_EINVAL;
+  return launch_pack_fp8(w, rows, cols, codes, scales, stream) ? MK_ECUDA : MK_OK;
+}
+
+int mk_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales, float* tscale, void* stream) {
+  if (!w || !codes || !bscales || !tscale || rows < 1 || cols < 16 || cols % 16) return MK_EINVAL;
+  return launch_pack_nvfp4(w, rows, cols, codes, bscales, tscale, stream) ? MK_ECUDA : MK_OK;
+}
+
+int mk_gemv(const mk_mat* w, int rows, int cols, const float* x, float* y, void* stream) {
+  if (!w || !x || !y || rows < 1 || cols < 1024 || cols % 1024 || cols > XS_MAX) return MK_EINVAL;
+  if (w->fmt < 0 || w->fmt > 2 || !w->data || !aligned16(w->data)) return MK_EINVAL;
+  if (w->fmt != MK_BF16 && (!w->scale || !aligned16(w->scale))) return MK_EINVAL;
+  int grid;
+  if (device_grid(&grid)) return MK_ECUDA;
+  return launch_gemv(to_dmat(*w), rows, cols, x, y, grid, stream) ? MK_ECUDA : MK_OK;
+}
+
+int mk_stream_read(const void* buf, size_t bytes, void* stream) {
+  int grid;
+  if (device_grid(&grid)) return MK_ECUDA;
+  const size_t unit = (size_t)16384 * grid;
+  if (!buf || !aligned16(buf) || bytes == 0 || bytes % unit) return MK_EINVAL;
+  return launch_stream_read(buf, bytes, grid, stream) ? MK_ECUDA : MK_OK;
+}
+
+int mk_probe_cvt(uint32_t* a, uint32_t* b, const float* in, int n, uint16_t* e4, uint8_t* e2, void* stream) {
+  if (n < 0 || (in && n % 2)) return MK_EINVAL;
+  return launch_probe_cvt(a, b, in, n, e4, e2, stream) ? MK_ECUDA : MK_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,112 @@
+// Definitions shared by the kernels (mk_kernel.cu, mk_aux.cu) and the host ABI (mk_api.cu).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+
+namespace mk {
+
+// Qwen3-0.6B shape family (monolith page, "Upstream facts", model bullet).
+constexpr int HID = 1024, NQH = 16, NKVH = 8, HD = 128, FFN = 3072;
+constexpr int QROWS = NQH * HD;                 // 2048
+constexpr int KVROWS = NKVH * HD;               // 1024
+constexpr int QKV_ROWS = QROWS + 2 * KVROWS;    // 4096
+constexpr int GQA = NQH / NKVH;                 // 2 query heads per KV head
+
+// Persistent CTA shape: 16 consumer warps + 1 producer warp.
+constexpr int NCW = 16;
+constexpr int NCT = NCW * 32;
+constexpr int NTHREADS = NCT + 32;
+
+// Shared-memory weight ring.
+constexpr int SLOT = 16384;
+constexpr int NSLOT = 11;
+constexpr int KVT = 32;                         // positions per KV tile (K 8 KB + V 8 KB)
+constexpr int UNIT_TILES = 9;                   // KV tiles an attention unit holds at once
+constexpr int UNIT_POS = KVT * UNIT_TILES;      // 288 positions per attention unit
+constexpr int MAXC = 32;                        // attention units per KV head, upper bound
+constexpr int XS_MAX = 4096;                    // floats of staged GEMV input
+constexpr int PART_STRIDE = 132;                // floats per attention partial (m, l, pad, acc[128])
+
+enum Phase { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_GATEUP = 3, PH_DOWN = 4, PH_HEAD = 5, PH_EMBED = 6,
+             PH_WAIT = 7, PH_COUNT = 8 };
+enum MatIdx { M_Q = 0, M_K, M_V, M_O, M_GATE, M_UP, M_DOWN };
+
+struct DMat {
+  const uint8_t* data;
+  const uint8_t* scale;
+  float tscale;
+  int fmt;
+};
+
+struct DLayer {
+  DMat m[7];
+  const uint16_t* ln_in;
+  const uint16_t* ln_post;
+  const uint16_t* q_norm;
+  const uint16_t* k_norm;
+};
+
+// Sync words, each on its own 128-byte line.
+struct SyncBlock {
+  uint32_t c[8][32];           // per-phase arrival counters (reset by the last CTA of a step)
+  uint32_t grp[NKVH][32];      // attention units finished, per KV head
+  unsigned long long key[16];  // packed (logit, index) argmax key
+  uint32_t status[32];         // [0] status code, [1] detail word, [2] abort flag
+  int32_t tok[32];             // [0] token produced by the last step
+};
+
+// X-ray record (24 bytes).
+struct TraceRec {
+  unsigned long long gtime;
+  unsigned long long clk;
+  uint32_t smid;
+  uint16_t cta;
+  uint8_t phase;
+  uint8_t kind;  // 0 = phase begin, 1 = phase end, 2 = wait begin, 3 = wait end
+};
+constexpr int TRACE_PER_CTA = 512;
+
+struct KParams {
+  const DLayer* layers;
+  int n_layers;
+  DMat embed;
+  const uint16_t* final_norm;
+  int vocab;
+  int max_ctx;
+  float eps;
+  uint16_t* kc;          // bf16 [L][NKVH][max_ctx][HD]
+  uint16_t* vc;
+  const float* rope_cos; // [max_ctx][HD/2]
+  const float* rope_sin;
+  float* h_mlp;          // residual after the MLP block (layer output) [HID]
+  float* h_attn;         // residual after the attention block [HID]
+  float* qkv;            // raw q|k|v [QKV_ROWS]
+  float* att;            // attention output [QROWS]
+  float* act;            // SwiGLU output [FFN]
+  float* attp;           // attention partials [NKVH][MAXC][2][PART_STRIDE]
+  SyncBlock* sync;
+  float* hidden_dbg;     // nullable [(L+1)][HID]
+  float* logits;         // nullable [vocab]
+  TraceRec* trace;       // nullable [grid][TRACE_PER_CTA]
+  int token;
+  const int32_t* token_ptr;  // nullable: read the input token here instead
+  int pos;
+  int32_t* next_out;
+  int units;             // attention units per KV head this step
+  unsigned long long timeout_ns;
+  int fault_cta;         // test hook (-1 = off)
+  int fault_phase;
+};
+
+// Launchers (mk_kernel.cu / mk_aux.cu)
+int launch_decode(const KParams& p, int grid, bool xray, void* stream);
+int decode_smem_bytes();
+int launch_gemv(const DMat& m, int rows, int cols, const float* x, float* y, int grid, void* stream);
+int launch_stream_read(const void* buf, size_t bytes, int grid, void* stream);
+int launch_rope_table(float* cosb, float* sinb, int max_ctx, float theta, void* stream);
+int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, void* stream);
+int launch_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
+int launch_probe_cvt(uint32_t* a, uint32_t* b, const float* in, int n, uint16_t* e4, uint8_t* e2, void* stream);
+int decode_occupancy(int* blocks_per_sm);
+
+}  // namespace mk

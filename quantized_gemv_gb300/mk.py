@@ -1,0 +1,294 @@
+"""Python binding of libmk.so (include/mk.h): argument marshalling only.
+
+Every step of the decode path runs in the library's CUDA kernels; PyTorch provides device
+memory and the stream. Importing this module loads (building if needed) the CUDA library and
+raises if it cannot: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+import numpy as np
+import torch
+
+from . import build as _build
+from .synthetic import FMT_BF16, FMT_FP8_ROW, FMT_NVFP4, LINEARS, ModelConfig
+
+MK_OK, MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, MK_ENOTRACE = 0, -1, -2, -3, -4, -5
+MK_FLAG_XRAY = 1
+ERRNAMES = {MK_EINVAL: "MK_EINVAL", MK_ECUDA: "MK_ECUDA", MK_ETIMEOUT: "MK_ETIMEOUT",
+            MK_ENORESIDENT: "MK_ENORESIDENT", MK_ENOTRACE: "MK_ENOTRACE"}
+TRACE_DTYPE = np.dtype([("gtime", "<u8"), ("clk", "<u8"), ("smid", "<u4"), ("cta", "<u2"),
+                        ("phase", "u1"), ("kind", "u1")])
+PHASES = {0: "qkv", 1: "attention", 2: "o_proj", 3: "gate_up", 4: "down", 5: "lm_head", 6: "embed"}
+
+
+class MkError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{ERRNAMES.get(code, code)}: {msg}")
+        self.code = code
+
+
+class mk_mat(C.Structure):
+    _fields_ = [("data", C.c_void_p), ("scale", C.c_void_p), ("tensor_scale", C.c_float), ("fmt", C.c_int)]
+
+
+class mk_config(C.Structure):
+    _fields_ = [("n_layers", C.c_int), ("hidden", C.c_int), ("n_q_heads", C.c_int), ("n_kv_heads", C.c_int),
+                ("head_dim", C.c_int), ("ffn", C.c_int), ("vocab", C.c_int), ("max_ctx", C.c_int),
+                ("rope_theta", C.c_float), ("rms_eps", C.c_float)]
+
+
+class mk_layer(C.Structure):
+    _fields_ = [("q", mk_mat), ("k", mk_mat), ("v", mk_mat), ("o", mk_mat), ("gate", mk_mat), ("up", mk_mat),
+                ("down", mk_mat), ("ln_in", C.c_void_p), ("ln_post", C.c_void_p), ("q_norm", C.c_void_p),
+                ("k_norm", C.c_void_p)]
+
+
+class mk_weights(C.Structure):
+    _fields_ = [("layers", C.c_void_p), ("embed", mk_mat), ("final_norm", C.c_void_p)]
+
+
+# every symbol include/mk.h declares
+EXPORTS = ("mk_max_context", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
+           "mk_decode_greedy", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
+           "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_gemv", "mk_stream_read", "mk_probe_cvt")
+
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = C.CDLL(path)
+        vp, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
+        L.mk_max_context.restype = C.c_int
+        L.mk_workspace_bytes.restype = sz
+        L.mk_workspace_bytes.argtypes = [C.POINTER(mk_config), C.c_uint]
+        L.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), vp, sz, vp, C.c_uint, C.POINTER(vp)]
+        L.mk_destroy.argtypes = [vp]
+        L.mk_last_error.restype = C.c_char_p
+        L.mk_last_error.argtypes = [vp]
+        L.mk_decode_step.argtypes = [vp, i32, i32, C.POINTER(i32), vp]
+        L.mk_decode_greedy.argtypes = [vp, i32, i32, i32, vp]
+        L.mk_sync.argtypes = [vp]
+        L.mk_kv_cache.argtypes = [vp, C.c_int, C.POINTER(vp), C.POINTER(vp)]
+        L.mk_debug_hidden.argtypes = [vp, vp]
+        L.mk_trace_dump.argtypes = [vp, vp, sz, C.POINTER(sz)]
+        L.mk_debug_fault.argtypes = [vp, C.c_int, C.c_int, C.c_int]
+        L.mk_pack_fp8_row.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp]
+        L.mk_pack_nvfp4.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
+        L.mk_gemv.argtypes = [C.POINTER(mk_mat), C.c_int, C.c_int, vp, vp, vp]
+        L.mk_stream_read.argtypes = [vp, sz, vp]
+        L.mk_probe_cvt.argtypes = [vp, vp, vp, C.c_int, vp, vp, vp]
+        _lib = L
+    return _lib
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _check(rc, handle=None, what=""):
+    if rc != MK_OK:
+        msg = lib().mk_last_error(handle).decode() if handle is not None or rc != MK_EINVAL else ""
+        raise MkError(rc, f"{what} {msg}".strip())
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("expected a CUDA tensor")
+
+
+# ------------------------------------------------------------------ building blocks
+class PackedMat:
+    """A packed weight matrix in device memory (keeps its tensors alive)."""
+
+    def __init__(self, fmt, rows, cols, data, scale=None, tensor_scale=0.0):
+        self.fmt, self.rows, self.cols = fmt, rows, cols
+        self.data, self.scale, self.tensor_scale = data, scale, float(tensor_scale)
+
+    def c(self) -> mk_mat:
+        return mk_mat(self.data.data_ptr(), None if self.scale is None else self.scale.data_ptr(),
+                      self.tensor_scale, self.fmt)
+
+
+def pack_fp8_row(w_bf16: torch.Tensor, stream=None):
+    _need_cuda(w_bf16)
+    rows, cols = w_bf16.shape
+    codes = torch.empty((rows, cols), dtype=torch.uint8, device=w_bf16.device)
+    scales = torch.empty(rows, dtype=torch.float32, device=w_bf16.device)
+    _check(lib().mk_pack_fp8_row(_ptr(w_bf16.contiguous()), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)),
+           what="mk_pack_fp8_row")
+    return codes, scales
+
+
+def pack_nvfp4(w_bf16: torch.Tensor, stream=None):
+    _need_cuda(w_bf16)
+    rows, cols = w_bf16.shape
+    dev = w_bf16.device
+    codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
+    bscales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
+    t = torch.empty(1, dtype=torch.float32, device=dev)
+    _check(lib().mk_pack_nvfp4(_ptr(w_bf16.contiguous()), rows, cols, _ptr(codes), _ptr(bscales), _ptr(t),
+                               _stream(stream)), what="mk_pack_nvfp4")
+    return codes, bscales, t
+
+
+def pack(w_bf16: torch.Tensor, fmt: int, stream=None) -> PackedMat:
+    rows, cols = w_bf16.shape
+    if fmt == FMT_BF16:
+        return PackedMat(fmt, rows, cols, w_bf16.contiguous())
+    if fmt == FMT_FP8_ROW:
+        c, s = pack_fp8_row(w_bf16, stream)
+        return PackedMat(fmt, rows, cols, c, s)
+    c, b, t = pack_nvfp4(w_bf16, stream)
+    torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
+    return PackedMat(fmt, rows, cols, c, b, float(t.item()))
+
+
+def gemv(m: PackedMat, x: torch.Tensor, stream=None) -> torch.Tensor:
+    _need_cuda(x)
+    y = torch.empty(m.rows, dtype=torch.float32, device=x.device)
+    mc = m.c()
+    _check(lib().mk_gemv(C.byref(mc), m.rows, m.cols, _ptr(x.contiguous()), _ptr(y), _stream(stream)),
+           what="mk_gemv")
+    return y
+
+
+def stream_read(buf: torch.Tensor, nbytes: int | None = None, stream=None):
+    _check(lib().mk_stream_read(_ptr(buf), buf.numel() * buf.element_size() if nbytes is None else nbytes,
+                                _stream(stream)), what="mk_stream_read")
+
+
+def probe_cvt(x_f32: torch.Tensor | None = None, stream=None):
+    dev = torch.device("cuda")
+    a = torch.empty(65536, dtype=torch.int32, device=dev)
+    b = torch.empty(256, dtype=torch.int32, device=dev)
+    n = 0 if x_f32 is None else x_f32.numel()
+    e4 = torch.empty(max(n // 2, 1), dtype=torch.int16, device=dev)
+    e2 = torch.empty(max(n // 2, 1), dtype=torch.uint8, device=dev)
+    _check(lib().mk_probe_cvt(_ptr(a), _ptr(b), _ptr(x_f32), n, _ptr(e4) if n else None, _ptr(e2) if n else None,
+                              _stream(stream)), what="mk_probe_cvt")
+    return a, b, e4[: n // 2], e2[: n // 2]
+
+
+def max_context() -> int:
+    return lib().mk_max_context()
+
+
+# ------------------------------------------------------------------ the model
+class Model:
+    """A decode engine instance over packed device weights.
+
+    `packed` = {"layers": [{name: PackedMat for LINEARS, "ln_in", "ln_post", "q_norm", "k_norm": bf16
+    tensors}], "embed": PackedMat, "final_norm": bf16 tensor}, all on the current CUDA device.
+    """
+
+    def __init__(self, cfg: ModelConfig, packed, flags: int = 0, stream=None):
+        self.cfg = cfg
+        self.packed = packed
+        self.flags = flags
+        self.stream = stream if stream is not None else torch.cuda.current_stream()
+        L = lib()
+        self._cfg = mk_config(cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn,
+                              cfg.vocab, cfg.max_ctx, cfg.rope_theta, cfg.rms_eps)
+        layers = (mk_layer * cfg.n_layers)()
+        for i, Lp in enumerate(packed["layers"]):
+            layers[i] = mk_layer(*(Lp[n].c() for n in LINEARS), Lp["ln_in"].data_ptr(), Lp["ln_post"].data_ptr(),
+                                 Lp["q_norm"].data_ptr(), Lp["k_norm"].data_ptr())
+        self._layers = layers
+        self._w = mk_weights(C.cast(layers, C.c_void_p), packed["embed"].c(), packed["final_norm"].data_ptr())
+        nbytes = L.mk_workspace_bytes(C.byref(self._cfg), flags)
+        if nbytes == 0:
+            raise MkError(MK_EINVAL, "mk_workspace_bytes rejected the config")
+        self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        h = C.c_void_p()
+        rc = L.mk_create(C.byref(self._cfg), C.byref(self._w), _ptr(self.workspace), nbytes,
+                         C.c_void_p(self.stream.cuda_stream), flags, C.byref(h))
+        if rc != MK_OK:
+            raise MkError(rc, L.mk_last_error(None).decode())
+        self.h = h
+        self._next = C.c_int32()
+
+    def close(self):
+        if getattr(self, "h", None):
+            lib().mk_destroy(self.h)
+            self.h = None
+
+    __del__ = close
+
+    def _err(self, rc, what):
+        if rc != MK_OK:
+            raise MkError(rc, f"{what}: {lib().mk_last_error(self.h).decode()}")
+
+    def decode_step(self, token: int, pos: int, logits: torch.Tensor | None = None) -> int:
+        rc = lib().mk_decode_step(self.h, int(token), int(pos), C.byref(self._next), _ptr(logits))
+        self._err(rc, "mk_decode_step")
+        return int(self._next.value)
+
+    def decode_greedy(self, first_token: int, pos0: int, n: int, out: torch.Tensor | None = None) -> torch.Tensor:
+        if out is None:
+            out = torch.empty(n, dtype=torch.int32, device="cuda")
+        self._err(lib().mk_decode_greedy(self.h, int(first_token), int(pos0), int(n), _ptr(out)), "mk_decode_greedy")
+        return out
+
+    def sync(self):
+        self._err(lib().mk_sync(self.h), "mk_sync")
+
+    def kv_cache(self, layer: int):
+        """(K, V) bf16 views [n_kv_heads][max_ctx][head_dim] into the model's workspace."""
+        k, v = C.c_void_p(), C.c_void_p()
+        self._err(lib().mk_kv_cache(self.h, layer, C.byref(k), C.byref(v)), "mk_kv_cache")
+        c = self.cfg
+        n = c.n_kv_heads * c.max_ctx * c.head_dim
+        base = self.workspace.data_ptr()
+        ws = self.workspace
+        kt = ws[k.value - base: k.value - base + 2 * n].view(torch.bfloat16).view(c.n_kv_heads, c.max_ctx, c.head_dim)
+        vt = ws[v.value - base: v.value - base + 2 * n].view(torch.bfloat16).view(c.n_kv_heads, c.max_ctx, c.head_dim)
+        return kt, vt
+
+    def hidden(self) -> torch.Tensor:
+        out = torch.empty((self.cfg.n_layers + 1, self.cfg.hidden), dtype=torch.float32, device="cuda")
+        self._err(lib().mk_debug_hidden(self.h, _ptr(out)), "mk_debug_hidden")
+        return out
+
+    def trace(self) -> np.ndarray:
+        cap = 0
+        grid = torch.cuda.get_device_properties(0).multi_processor_count
+        cap = grid * 512 * TRACE_DTYPE.itemsize
+        buf = np.zeros(cap, dtype=np.uint8)
+        written = C.c_size_t()
+        self._err(lib().mk_trace_dump(self.h, buf.ctypes.data_as(C.c_void_p), cap, C.byref(written)), "mk_trace_dump")
+        return buf[: written.value].view(TRACE_DTYPE).reshape(grid, 512)
+
+    def debug_fault(self, cta: int, phase: int, timeout_ms: int = 0):
+        self._err(lib().mk_debug_fault(self.h, cta, phase, timeout_ms), "mk_debug_fault")
+
+
+def upload_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+def pack_model(master, fmap, device="cuda"):
+    """Upload bf16 master weights and quantise them on the device with the library's packers."""
+    def pk(bits, fmt):
+        return pack(upload_bf16(bits, device), fmt)
+
+    out = {"embed": pk(master["embed"], fmap["embed"]), "final_norm": upload_bf16(master["final_norm"], device),
+           "layers": []}
+    for L in master["layers"]:
+        d = {n: pk(L[n], fmap[n]) for n in LINEARS}
+        for n in ("ln_in", "ln_post", "q_norm", "k_norm"):
+            d[n] = upload_bf16(L[n], device)
+        out["layers"].append(d)
+    torch.cuda.synchronize()
+    return out
