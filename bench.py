@@ -1,0 +1,400 @@
+"""Benchmark: batch-1 greedy decode of a Qwen3-0.6B-shaped model, one megakernel launch per token.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+A "step" is one decode step: one launch of the decode kernel producing one token (embedding,
+28 layers, final norm, LM head and argmax). The timed region holds exactly K steps (positions
+P..P+K-1 after the workload's 32-token prompt or prefilled KV), launched back to back with the
+input token of each launch read from device memory; it is bracketed by a barrier and
+torch.cuda.synchronize() and timed with CUDA events on the launching stream. Warm-up runs the
+same positions W times first. Every step streams >= 0.4 GB of weights, far above the 135 MB L2,
+so no L2 flush is needed between steps.
+
+Extra keys beyond the base contract: `roofline` (the decode kernel against the measured HBM copy
+bandwidth), `cpu_baseline` (the CPU oracle on this host's cores, a bounded sample), `e2e` (the
+same metric through mk_decode_step, which returns each token to the host), `clocks` (NVML samples
+during the timed region), `stream_read_gbs` (the library's bulk-copy streaming-read probe, same
+run) and `variants` (the FP8, NVFP4 and long-context FP8 workloads, each timed the same way).
+
+--impl reference times the CPU oracle (the only reference implementation of this method) on the
+same workload and prints its line with "impl": "reference". Under torchrun, rank 0 alone runs it.
+Multi-GPU: each rank decodes its own independent replica (the path has no data-parallel
+exchange); value = tokens of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from quantized_gemv_gb300 import synthetic as S  # noqa: E402
+
+HEADLINE = "qwen3_0.6b_bf16"
+UPSTREAM_BF16_TOKS = 1033.0  # RTX 5090 upstream kernel, bf16 (monolith page, "Upstream facts")
+
+
+# ------------------------------------------------------------------ byte accounting
+def weight_bytes(cfg: S.ModelConfig, variant: str) -> int:
+    """Bytes of every weight and scale one decode step reads (embedding row excluded)."""
+    fmap = S.format_map(variant)
+    per = {S.FMT_BF16: lambda r, c: 2 * r * c, S.FMT_FP8_ROW: lambda r, c: r * c + 4 * r,
+           S.FMT_NVFP4: lambda r, c: r * c // 2 + r * c // 16 + 4}
+    total = 0
+    for name, (r, c) in cfg.shapes().items():
+        total += per[fmap[name]](r, c)
+    total += 2 * (2 * cfg.hidden + 2 * cfg.head_dim)  # norm weights
+    total *= cfg.n_layers
+    total += per[fmap["embed"]](cfg.vocab, cfg.hidden) + 2 * cfg.hidden  # LM head + final norm
+    return total
+
+
+def kv_bytes(cfg: S.ModelConfig, pos: int) -> int:
+    """KV-cache bytes one step at `pos` reads (positions 0..pos-1) and writes (position pos)."""
+    per_pos = cfg.n_layers * cfg.n_kv_heads * cfg.head_dim * 2 * 2
+    return per_pos * (pos + 1)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d.get("hbm_gbs", 6800.0)), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "quantized_gemv_gb300", "csrc")
+    for n in sorted(os.listdir(csrc)):
+        if n.startswith("mk_kernel") or n.endswith((".cuh", ".h")):
+            with open(os.path.join(csrc, n), "rb") as f:
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    path = os.path.join(ROOT, "profiles", "decode_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("kernel_hash") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------------ clocks (read-only NVML)
+class ClockSampler:
+    """Samples SM clock and clock-event reasons through NVML (read-only queries) in a thread."""
+    REASONS = {0x1: "gpu_idle", 0x2: "applications_clocks", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake",
+               0x100: "display_clocks"}
+
+    def __init__(self, index: int):
+        self.ok = False
+        self.samples = []
+        try:
+            self.nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.nv.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            p = torch.cuda.get_device_properties(index)
+            bus = f"{p.pci_domain_id:08x}:{p.pci_bus_id:02x}:{p.pci_device_id:02x}.0".encode()
+            if self.nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(self.h)) != 0:
+                return
+            self.read()
+            self.ok = True
+        except (OSError, AttributeError):
+            self.ok = False
+
+    def read(self):
+        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))       # NVML_CLOCK_SM
+        self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
+        self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
+        return clk.value, mx.value, rs.value
+
+    def __enter__(self):
+        self._stop = False
+        if self.ok:
+            self.samples.append(self.read())
+
+            def loop():
+                while not self._stop:
+                    self.samples.append(self.read())
+                    time.sleep(0.002)
+            self.t = threading.Thread(target=loop, daemon=True)
+            self.t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop = True
+        if self.ok:
+            self.t.join()
+            self.samples.append(self.read())
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
+        reasons = set()
+        for _, _, r in self.samples:
+            for bit, name in self.REASONS.items():
+                if r & bit and name != "gpu_idle":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[0] for s in self.samples),
+                "sm_max_mhz": max(s[1] for s in self.samples), "samples": len(self.samples),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ GPU arm
+def setup_model(wl: S.Workload, mk):
+    cfg = wl.config()
+    master = S.master_weights(cfg, seed=0)
+    packed = mk.pack_model(master, S.format_map(wl.variant))
+    model = mk.Model(cfg, packed)
+    start_pos = 0
+    if wl.prefill:
+        k, v = S.prefill_kv(cfg, wl.prefill, seed=2)
+        for l in range(cfg.n_layers):
+            kt, vt = model.kv_cache(l)
+            kt[:, : wl.prefill].copy_(mk.upload_bf16(k[l]))
+            vt[:, : wl.prefill].copy_(mk.upload_bf16(v[l]))
+        start_pos = wl.prefill
+        first = int(S.prompt_ids(cfg, 1)[0])
+    else:
+        prompt = S.prompt_ids(cfg, wl.prompt_len)
+        tok = int(prompt[0])
+        for pos in range(wl.prompt_len):  # prompt fed token by token, untimed
+            nxt = model.decode_step(tok, pos)
+            tok = int(prompt[pos + 1]) if pos + 1 < wl.prompt_len else nxt
+        start_pos = wl.prompt_len
+        first = tok
+    torch.cuda.synchronize()
+    return cfg, master, model, start_pos, first
+
+
+def time_steps(model, first: int, pos0: int, k: int, warmup: int, dist=None):
+    """Time exactly k launches; returns (total_ms, per-launch ms list, tokens)."""
+    dev = torch.device("cuda")
+    toks = torch.zeros(k + 1, dtype=torch.int32, device=dev)
+    stream = model.stream
+
+    def run(n):
+        toks[0] = first
+        for i in range(n):
+            model.decode_next(toks[i: i + 1], pos0 + i, toks[i + 1: i + 2])
+
+    for _ in range(max(warmup, 0)):
+        run(min(k, 8))
+    model.sync()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(k + 1)]
+    toks[0] = first
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        for i in range(k):
+            ev[i].record(stream)
+            model.decode_next(toks[i: i + 1], pos0 + i, toks[i + 1: i + 2])
+        ev[k].record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    model.sync()
+    per = [ev[i].elapsed_time(ev[i + 1]) for i in range(k)]
+    total = ev[0].elapsed_time(ev[k])
+    return total, per, toks[1:].cpu().numpy()
+
+
+def time_e2e(model, first: int, pos0: int, k: int):
+    """Per-token host loop through mk_decode_step: the token goes in with the launch and comes back
+    to the host before the next step is issued."""
+    tok = first
+    model.decode_step(tok, pos0)  # warm
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(k):
+        tok = model.decode_step(tok, pos0 + i)
+    return (time.perf_counter() - t0) * 1e3
+
+
+def stream_read_gbs(mk):
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    unit = 16384 * sms
+    n = (2 << 30) // unit * unit
+    buf = torch.empty(n, dtype=torch.uint8, device="cuda")
+    for _ in range(3):
+        mk.stream_read(buf)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    best = 1e9
+    for _ in range(5):
+        e0.record()
+        mk.stream_read(buf)
+        e1.record()
+        torch.cuda.synchronize()
+        best = min(best, e0.elapsed_time(e1))
+    del buf
+    return n / (best * 1e-3) / 1e9
+
+
+def oracle_sample(wl: S.Workload, master, seconds: float = 12.0):
+    """The CPU oracle decoding the same workload on this host's cores: steps until `seconds`."""
+    from oracle import oracle as O
+    cfg = wl.config()
+    cores = len(os.sched_getaffinity(0))
+    packed = O.pack_model(master, S.format_map(wl.variant), cores)
+    om = O.OracleModel(cfg, packed, n_threads=cores)
+    if wl.prefill:
+        k, v = S.prefill_kv(cfg, wl.prefill, seed=2)
+        om.set_kv(k, v)
+        pos, tok = wl.prefill, int(S.prompt_ids(cfg, 1)[0])
+    else:
+        pos, tok = 0, int(S.prompt_ids(cfg, 1)[0])
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        tok, _, _, _ = om.step(tok, pos, want_logits=False)
+        pos += 1
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds and steps >= 2:
+            break
+    return {"value": steps / el, "unit": "tok/s", "cores": cores, "kind": "oracle",
+            "sample": f"{steps} greedy steps of {wl.name} from position {0 if not wl.prefill else wl.prefill} "
+                      f"({el:.1f} s, double precision, {cores} threads)"}
+
+
+def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_steps: int | None = None):
+    cfg, master, model, pos0, first = setup_model(wl, mk)
+    k = steps
+    if pos0 + k > cfg.max_ctx:
+        raise SystemExit(f"{wl.name}: {k} steps from position {pos0} exceed max_ctx {cfg.max_ctx}")
+    sampler = ClockSampler(torch.cuda.current_device())
+    with sampler:
+        total_ms, per, toks = time_steps(model, first, pos0, k, warmup, dist)
+    e2e_ms = time_e2e(model, first, pos0, e2e_steps or k)
+    wbytes = weight_bytes(cfg, wl.variant)
+    mean_pos = pos0 + (k - 1) / 2
+    launch_ms = float(np.mean(per))
+    res = {"tok_s": k / (total_ms * 1e-3), "ms_per_step": total_ms / k, "launch_ms": launch_ms,
+           "weight_bytes": wbytes, "kv_bytes": kv_bytes(cfg, int(round(mean_pos))),
+           "e2e_tok_s": (e2e_steps or k) / (e2e_ms * 1e-3), "clocks": sampler.summary(),
+           "first_tokens": toks[:4].tolist()}
+    res["weight_gbs"] = wbytes / (launch_ms * 1e-3) / 1e9
+    res["total_gbs"] = (wbytes + res["kv_bytes"]) / (launch_ms * 1e-3) / 1e9
+    model.close()
+    return res, master
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=128)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=HEADLINE, choices=sorted(S.WORKLOADS))
+    ap.add_argument("--impl", default="engine", choices=["engine", "reference"])
+    ap.add_argument("--no-variants", action="store_true", help="skip the FP8/NVFP4/long-context lines")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist = None
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("gloo")
+        dist = tdist
+    wl = S.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        master = S.master_weights(wl.config(), seed=0)
+        cb = oracle_sample(wl, master, seconds=20.0)
+        line = {"metric": "batch-1 decode tok/s (Qwen3-0.6B shape)", "value": cb["value"], "unit": "tok/s",
+                "impl": "reference", "n_gpus": 0, "steps": None, "warmup": 0, "higher_is_better": True,
+                "dtype": "f64", "data": "synthetic (seeded random weights, uniform prompt ids)",
+                "config": {"workload": wl.name, "description": wl.description},
+                "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
+                                            "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    torch.cuda.set_device(local)
+    from quantized_gemv_gb300 import mk
+    stream_gbs = stream_read_gbs(mk) if rank == 0 else None
+    res, master = run_workload(wl, args.steps, args.warmup, mk, dist)
+    # whole-job value: tokens of all replicas over the slowest replica's time
+    total_ms = res["ms_per_step"] * args.steps
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = world * args.steps / (total_ms * 1e-3)
+    peak, peak_kind = measured_peaks()
+    achieved = (res["weight_bytes"] + res["kv_bytes"]) / (res["launch_ms"] * 1e-3) / 1e9
+    variants = {}
+    if not args.no_variants and rank == 0:
+        for name in ("qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4", "qwen3_0.6b_fp8_ctx4096"):
+            if name == wl.name:
+                continue
+            w2 = S.WORKLOADS[name]
+            r2, _ = run_workload(w2, min(args.steps, w2.steps), args.warmup, mk, None, e2e_steps=16)
+            variants[name] = {"tok_s": round(r2["tok_s"], 1), "ms_per_step": round(r2["ms_per_step"], 4),
+                              "weight_gbs": round(r2["weight_gbs"], 1),
+                              "roofline_frac_weights": round(r2["weight_gbs"] / peak, 4),
+                              "roofline_frac_weights_kv": round(r2["total_gbs"] / peak, 4),
+                              "e2e_tok_s": round(r2["e2e_tok_s"], 1), "clocks": r2["clocks"]}
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_sample(wl, master, seconds=12.0)
+    if rank != 0:
+        return
+    line = {
+        "metric": "batch-1 decode tok/s (Qwen3-0.6B shape)", "value": round(value, 2), "unit": "tok/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": round(value / world / UPSTREAM_BF16_TOKS, 3) if wl.name == HEADLINE else None,
+        "dtype": "f32", "weights": wl.variant,
+        "data": "synthetic (seeded N(0,0.02) bf16 weights, uniform prompt ids)",
+        "config": {"workload": wl.name, "description": wl.description, "model": "Qwen3-0.6B shape, random init",
+                   "global_batch": world, "positions": f"{S.WORKLOADS[wl.name].prompt_len + wl.prefill}.."
+                   f"{S.WORKLOADS[wl.name].prompt_len + wl.prefill + args.steps - 1}",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "no flush: every step reads >= 0.4 GB of weights, L2 is 135 MB"},
+        "weight_stream_gbs": round(res["weight_gbs"], 1),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl.name),
+                     "kernel": "mk::k_decode", "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": res["weight_bytes"] + res["kv_bytes"],
+                     "launch_ms": round(res["launch_ms"], 5)},
+        "stream_read_gbs": round(stream_gbs, 1) if stream_gbs else None,
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(res["e2e_tok_s"], 2), "unit": "tok/s", "h2d_bytes_per_step": 4,
+                "d2h_bytes_per_step": 256, "api": "mk_decode_step (token in with the launch, status+token back)"},
+        "gpu_launches": args.steps,
+        "clocks": res["clocks"],
+        "variants": variants,
+    }
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

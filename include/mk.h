@@ -119,6 +119,11 @@ int mk_decode_step(mk_model* m, int32_t token, int32_t pos, int32_t* next_token_
  * synchronise; errors of the device steps are reported by the next mk_sync. */
 int mk_decode_greedy(mk_model* m, int32_t first_token, int32_t pos0, int32_t n, int32_t* tokens_dev);
 
+/* One decode launch without a host round trip: the input token is read from token_dev (device
+ * int32), the produced token is written to next_dev (device int32), optional logits to
+ * logits_dev. Does not synchronise; device-side errors are reported by the next mk_sync. */
+int mk_decode_next(mk_model* m, const int32_t* token_dev, int32_t pos, int32_t* next_dev, float* logits_dev);
+
 /* Wait for the model's stream and report any device-side status (e.g. MK_ETIMEOUT). */
 int mk_sync(mk_model* m);
 

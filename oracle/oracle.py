@@ -139,6 +139,28 @@ def pack(w_bf16: np.ndarray, fmt: int) -> PackedMat:
     return PackedMat(fmt, rows, cols, c, b, t)
 
 
+def pack_model(master, fmap, nthreads=None):
+    """Quantise every matrix of a bf16 master-weight dict with the oracle's own quantisers.
+    master: {"embed", "layers": [{"q".."down", "ln_in", "ln_post", "q_norm", "k_norm"}], "final_norm"}
+    fmap: {"embed": fmt, "q": fmt, ...}."""
+    def pk(w, fmt):
+        if fmt == FMT_BF16:
+            return PackedMat(fmt, w.shape[0], w.shape[1], w)
+        if fmt == FMT_FP8_ROW:
+            c, s = quant_fp8_row(w, nthreads)
+            return PackedMat(fmt, w.shape[0], w.shape[1], c, s)
+        c, b, t = quant_nvfp4(w, nthreads)
+        return PackedMat(fmt, w.shape[0], w.shape[1], c, b, t)
+
+    out = {"embed": pk(master["embed"], fmap["embed"]), "final_norm": master["final_norm"], "layers": []}
+    for L in master["layers"]:
+        d = {n: pk(L[n], fmap[n]) for n in LINEARS}
+        for n in ("ln_in", "ln_post", "q_norm", "k_norm"):
+            d[n] = L[n]
+        out["layers"].append(d)
+    return out
+
+
 def dequant(m: PackedMat) -> np.ndarray:
     out = np.zeros((m.rows, m.cols), np.float64)
     mc = m.c()

@@ -21,7 +21,9 @@ struct mk_model {
   // workspace carve-up (device)
   SyncBlock* sync;
   DLayer* dlayers;
-  float *h_mlp, *h_attn, *qkv, *att, *act, *attp;
+  llword *h_mlp, *h_attn, *qkv, *att, *act;
+  float* attp;
+  uint32_t steps;  // launches so far; tags of a launch start at 64 * steps
   float *rope_cos, *rope_sin;
   uint16_t *kc, *vc;
   float* hidden_dbg;
@@ -78,11 +80,11 @@ static bool layout_of(const mk_config* c, unsigned flags, int grid, Layout* L) {
   const size_t kv = (size_t)c->n_layers * NKVH * c->max_ctx * HD * sizeof(uint16_t);
   L->sync = take(sizeof(SyncBlock));
   L->layers = take(sizeof(DLayer) * c->n_layers);
-  L->h_mlp = take(HID * 4);
-  L->h_attn = take(HID * 4);
-  L->qkv = take(QKV_ROWS * 4);
-  L->att = take(QROWS * 4);
-  L->act = take(FFN * 4);
+  L->h_mlp = take(HID * sizeof(llword));
+  L->h_attn = take(HID * sizeof(llword));
+  L->qkv = take(QKV_ROWS * sizeof(llword));
+  L->att = take(QROWS * sizeof(llword));
+  L->act = take(FFN * sizeof(llword));
   L->attp = take((size_t)NKVH * MAXC * 2 * PART_STRIDE * 4);
   L->rope_cos = take((size_t)c->max_ctx * (HD / 2) * 4);
   L->rope_sin = take((size_t)c->max_ctx * (HD / 2) * 4);
@@ -195,11 +197,12 @@ int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes
   uint8_t* base = (uint8_t*)ws;
   m->sync = (SyncBlock*)(base + L.sync);
   m->dlayers = (DLayer*)(base + L.layers);
-  m->h_mlp = (float*)(base + L.h_mlp);
-  m->h_attn = (float*)(base + L.h_attn);
-  m->qkv = (float*)(base + L.qkv);
-  m->att = (float*)(base + L.att);
-  m->act = (float*)(base + L.act);
+  m->h_mlp = (llword*)(base + L.h_mlp);
+  m->h_attn = (llword*)(base + L.h_attn);
+  m->qkv = (llword*)(base + L.qkv);
+  m->att = (llword*)(base + L.att);
+  m->act = (llword*)(base + L.act);
+  m->steps = 0;
   m->attp = (float*)(base + L.attp);
   m->rope_cos = (float*)(base + L.rope_cos);
   m->rope_sin = (float*)(base + L.rope_sin);
@@ -238,11 +241,10 @@ void mk_destroy(mk_model* m) {
   delete m;
 }
 
+// Attention units per KV head for a step at `pos`: one unit when the whole context fits one
+// unit's shared-memory window (no merge step), else one unit per (SM / KV head).
 static int units_for(const mk_model* m, int pos) {
-  int u = (pos + 1 + KVT - 1) / KVT;
-  if (u > m->max_units) u = m->max_units;
-  if (u < 1) u = 1;
-  return u;
+  return (pos + 1 <= UNIT_POS) ? 1 : m->max_units;
 }
 
 static KParams base_params(mk_model* m) {
@@ -271,6 +273,13 @@ static KParams base_params(mk_model* m) {
   p.fault_cta = m->fault_cta;
   p.fault_phase = m->fault_phase;
   return p;
+}
+
+// Tags of one launch: 64 * (launch number) + layer; never 0 (the workspace starts zeroed).
+static uint32_t next_tagbase(mk_model* m) {
+  m->steps = (m->steps + 1) & 0x03FFFFFFu;
+  if (m->steps == 0) m->steps = 1;
+  return m->steps * 64u;
 }
 
 // Read the device status; on a failed step clear the sync block so the model stays usable.
@@ -309,6 +318,7 @@ int mk_decode_step(mk_model* m, int32_t token, int32_t pos, int32_t* next_token_
   p.next_out = nullptr;
   p.logits = logits_dev;
   p.units = units_for(m, pos);
+  p.tagbase = next_tagbase(m);
   if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
     return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
   return collect_status(m, next_token_host);
@@ -326,9 +336,26 @@ int mk_decode_greedy(mk_model* m, int32_t first_token, int32_t pos0, int32_t n, 
     p.next_out = tokens_dev + i;
     p.logits = nullptr;
     p.units = units_for(m, p.pos);
+    p.tagbase = next_tagbase(m);
     if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
       return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
   }
+  return MK_OK;
+}
+
+int mk_decode_next(mk_model* m, const int32_t* token_dev, int32_t pos, int32_t* next_dev, float* logits_dev) {
+  if (!m || !token_dev || !next_dev) return MK_EINVAL;
+  if (pos < 0 || pos >= m->cfg.max_ctx) return set_err(m, MK_EINVAL, "pos %d out of range", pos);
+  KParams p = base_params(m);
+  p.token = 0;
+  p.token_ptr = token_dev;
+  p.pos = pos;
+  p.next_out = next_dev;
+  p.logits = logits_dev;
+  p.units = units_for(m, pos);
+  p.tagbase = next_tagbase(m);
+  if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
+    return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
   return MK_OK;
 }
 

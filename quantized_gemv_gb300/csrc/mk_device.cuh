@@ -102,6 +102,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of a phase (never suspends the thread; callers spin on it).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{ .reg .pred p; mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+      : "=r"(ok)
+      : "r"(smem_u32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
@@ -132,37 +142,35 @@ __device__ __forceinline__ float2 e2m1x2_to_f2(uint32_t byte) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
-// 16 bytes of weights times the matching activations, accumulated into acc.
-// bf16: 8 weights, x: 2 float4.  FP8: 16 weights, x: 4 float4.
-__device__ __forceinline__ float dot_bf16_16B(uint4 w, const float4* x, float acc) {
+// 16 bytes of weights times the matching activations, accumulated into acc[0..1] (two independent
+// chains keep the FMA dependency short). bf16: 8 weights, x: 2 float4. FP8: 16 weights, x: 4 float4.
+__device__ __forceinline__ void dot_bf16_16B(uint4 w, const float4* x, float* acc) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float lo = __uint_as_float(ws[i] << 16), hi = __uint_as_float(ws[i] & 0xFFFF0000u);
     const float4 xv = x[i / 2];
     float xa = (i & 1) ? xv.z : xv.x, xb = (i & 1) ? xv.w : xv.y;
-    acc = fmaf(lo, xa, acc);
-    acc = fmaf(hi, xb, acc);
+    acc[0] = fmaf(lo, xa, acc[0]);
+    acc[1] = fmaf(hi, xb, acc[1]);
   }
-  return acc;
 }
-__device__ __forceinline__ float dot_fp8_16B(uint4 w, const float4* x, float acc) {
+__device__ __forceinline__ void dot_fp8_16B(uint4 w, const float4* x, float* acc) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     float2 a = e4m3x2_to_f2(ws[i] & 0xFFFFu), b = e4m3x2_to_f2(ws[i] >> 16);
     const float4 xv = x[i];
-    acc = fmaf(a.x, xv.x, acc);
-    acc = fmaf(a.y, xv.y, acc);
-    acc = fmaf(b.x, xv.z, acc);
-    acc = fmaf(b.y, xv.w, acc);
+    acc[0] = fmaf(a.x, xv.x, acc[0]);
+    acc[1] = fmaf(a.y, xv.y, acc[1]);
+    acc[0] = fmaf(b.x, xv.z, acc[0]);
+    acc[1] = fmaf(b.y, xv.w, acc[1]);
   }
-  return acc;
 }
 // NVFP4: 16 bytes = 32 weights = two 16-element scale blocks; x: 8 float4; s0/s1: block scales.
-__device__ __forceinline__ float dot_nvfp4_16B(uint4 w, const float4* x, float s0, float s1, float acc) {
+__device__ __forceinline__ void dot_nvfp4_16B(uint4 w, const float4* x, float s0, float s1, float* acc) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-  float blk[2] = {0.f, 0.f};
+  float blk[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
 #pragma unroll
@@ -171,13 +179,12 @@ __device__ __forceinline__ float dot_nvfp4_16B(uint4 w, const float4* x, float s
       const int e = i * 8 + b * 2;  // element index within the lane's 32
       const float4 xv = x[e / 4];
       float xa = (e % 4 == 0) ? xv.x : xv.z, xb = (e % 4 == 0) ? xv.y : xv.w;
-      blk[i / 2] = fmaf(v.x, xa, blk[i / 2]);
-      blk[i / 2] = fmaf(v.y, xb, blk[i / 2]);
+      blk[i / 2][0] = fmaf(v.x, xa, blk[i / 2][0]);
+      blk[i / 2][1] = fmaf(v.y, xb, blk[i / 2][1]);
     }
   }
-  acc = fmaf(blk[0], s0, acc);
-  acc = fmaf(blk[1], s1, acc);
-  return acc;
+  acc[0] = fmaf(blk[0][0] + blk[0][1], s0, acc[0]);
+  acc[1] = fmaf(blk[1][0] + blk[1][1], s1, acc[1]);
 }
 
 }  // namespace mk

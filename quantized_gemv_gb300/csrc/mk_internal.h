@@ -12,8 +12,11 @@ constexpr int KVROWS = NKVH * HD;               // 1024
 constexpr int QKV_ROWS = QROWS + 2 * KVROWS;    // 4096
 constexpr int GQA = NQH / NKVH;                 // 2 query heads per KV head
 
-// Persistent CTA shape: 16 consumer warps + 1 producer warp.
-constexpr int NCW = 16;
+// Persistent CTA shape: 8 consumer warps + 1 producer warp. Every GEMV phase of a CTA is small
+// (tens of rows), so its time goes to per-warp bookkeeping as much as to math: fewer warps, each
+// computing four rows at once, keep the SM's issue slots on the dot products. Nine warps leave
+// 168 registers per thread (no spills: with shared memory taking most of the SM, spills miss L1).
+constexpr int NCW = 8;
 constexpr int NCT = NCW * 32;
 constexpr int NTHREADS = NCT + 32;
 
@@ -66,6 +69,11 @@ struct TraceRec {
 };
 constexpr int TRACE_PER_CTA = 512;
 
+// Activations cross SMs as 64-bit words {fp32 value (low), u32 tag (high)} stored with one
+// single-copy-atomic 64-bit store: a consumer polls the words themselves until every one carries
+// the tag of the (step, layer) it needs, so no fence, counter or second round trip is involved.
+typedef unsigned long long llword;
+
 struct KParams {
   const DLayer* layers;
   int n_layers;
@@ -78,11 +86,11 @@ struct KParams {
   uint16_t* vc;
   const float* rope_cos; // [max_ctx][HD/2]
   const float* rope_sin;
-  float* h_mlp;          // residual after the MLP block (layer output) [HID]
-  float* h_attn;         // residual after the attention block [HID]
-  float* qkv;            // raw q|k|v [QKV_ROWS]
-  float* att;            // attention output [QROWS]
-  float* act;            // SwiGLU output [FFN]
+  llword* h_mlp;         // residual after the MLP block (layer output) [HID]
+  llword* h_attn;        // residual after the attention block [HID]
+  llword* qkv;           // raw q|k|v [QKV_ROWS]
+  llword* att;           // attention output [QROWS]
+  llword* act;           // SwiGLU output [FFN]
   float* attp;           // attention partials [NKVH][MAXC][2][PART_STRIDE]
   SyncBlock* sync;
   float* hidden_dbg;     // nullable [(L+1)][HID]
@@ -93,6 +101,7 @@ struct KParams {
   int pos;
   int32_t* next_out;
   int units;             // attention units per KV head this step
+  uint32_t tagbase;      // tag of layer l in this step = tagbase + l (unique per launch, never 0)
   unsigned long long timeout_ns;
   int fault_cta;         // test hook (-1 = off)
   int fault_phase;

@@ -6,11 +6,14 @@
 //     bf16 KV cache) with cp.async.bulk into an 11-slot shared-memory ring. Weights do not depend
 //     on the token, so the stream runs ahead across every wait ("productive spin", monolith page,
 //     "Upstream facts"; generalised from an L2 prefetch into staging in the SM's own memory);
-//   * 16 consumer warps dequantise the staged rows in registers (cvt e4m3x2 / e2m1x2 -> f16x2 ->
-//     fp32) and accumulate in fp32 with warp-shuffle reductions;
-//   * grid barriers are replaced by per-phase arrival counters written with release and polled
-//     with acquire at gpu scope ("Hazy-style counters", monolith page, "Design decisions", sync
-//     experiment 2), each wait bounded by a %globaltimer deadline;
+//   * 16 consumer warps each own whole rows: they dequantise the staged rows in registers (cvt
+//     e4m3x2 / e2m1x2 -> f16x2 -> fp32), keep the activation slice of a lane in registers, and
+//     accumulate in fp32 with one warp-shuffle reduction per row; warps take and release ring
+//     slots independently, so no CTA barrier sits inside a phase;
+//   * grid barriers are replaced by per-element readiness: every activation crosses SMs as a
+//     64-bit {value, tag} word and a consumer waits only on the words it reads (the counter idea
+//     of "Hazy-style counters", monolith page, "Design decisions", sync experiment 2, with the
+//     counter folded into the data), each wait bounded by a %globaltimer deadline;
 //   * the RMSNorm factor is recomputed by every CTA instead of meeting at a barrier (monolith
 //     page, "Upstream facts", tricks already in upstream);
 //   * attention is split over (KV head, position chunk) units; the last unit of a KV head to
@@ -26,12 +29,60 @@
 
 namespace mk {
 
+__device__ __forceinline__ void split_range(int n, int parts, int i, int& a, int& b) {
+  a = (int)((long long)n * i / parts);
+  b = (int)((long long)n * (i + 1) / parts);
+}
+
+// ------------------------------------------------------------------ per-CTA schedule
+// Both the producer and the consumers derive the same ranges, so they agree on the tile order.
+struct Sched {
+  int qm;        // which of q (0), k (1), v (2) this CTA's QKV rows belong to
+  int qr0, qr1;  // its rows of that matrix
+  int qbase;     // offset of that matrix's outputs in the q|k|v vector
+  int o0, o1;    // o_proj output rows
+  int j0, j1;    // FFN units (gate and up rows)
+  int d0, d1;    // down_proj output rows
+  int v0, v1;    // LM-head rows
+  bool unit;     // this CTA runs an attention unit
+  int ug, uc;    // its KV head and chunk
+  int t0, t1;    // positions [t0, t1) of the chunk
+  int ncached;   // positions of the chunk already in the cache (read through the ring)
+  __device__ void make(const KParams& P) {
+    const int G = gridDim.x, b = blockIdx.x;
+    // q, k and v rows go to disjoint CTA groups in proportion to their sizes (2 : 1 : 1), so every
+    // CTA streams rows of a single matrix
+    const int gq = G / 2, gk = G / 4, gv = G - gq - gk;
+    if (b < gq) {
+      qm = 0, qbase = 0;
+      split_range(QROWS, gq, b, qr0, qr1);
+    } else if (b < gq + gk) {
+      qm = 1, qbase = QROWS;
+      split_range(KVROWS, gk, b - gq, qr0, qr1);
+    } else {
+      qm = 2, qbase = QROWS + KVROWS;
+      split_range(KVROWS, gv, b - gq - gk, qr0, qr1);
+    }
+    split_range(HID, G, b, o0, o1);
+    split_range(FFN, G, b, j0, j1);
+    split_range(HID, G, b, d0, d1);
+    split_range(P.vocab, G, b, v0, v1);
+    unit = b < NKVH * P.units;
+    ug = unit ? b / P.units : 0;
+    uc = unit ? b % P.units : 0;
+    split_range(P.pos + 1, P.units, uc, t0, t1);
+    int c_end = t1 < P.pos ? t1 : P.pos;
+    ncached = unit ? (c_end > t0 ? c_end - t0 : 0) : 0;
+  }
+};
+
+constexpr int MAX_LAYERS = 64;
+constexpr int RS_MAX = 3 * NCT;
 struct __align__(16) Smem {
   uint64_t full[NSLOT];
   uint64_t empty[NSLOT];
   float xs[XS_MAX];
   float hs[HID];
-  float part[2][32][NCW];
   float gs[64];
   float us[64];
   float red[64];
@@ -40,11 +91,15 @@ struct __align__(16) Smem {
   float vn[HD];
   float sc[2][UNIT_POS];
   float stat[4];
+  float rs[RS_MAX];        // FP8 row scales of this CTA's rows in the current phase
+  DLayer lay[MAX_LAYERS];  // the layer table, copied once per launch
+  Sched sched;             // this CTA's row ranges and attention unit
   int flag;
   volatile int abort;
 };
 constexpr int RING_BYTES = SLOT * NSLOT;
 constexpr int SMEM_BYTES = RING_BYTES + (int)sizeof(Smem);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget of one CTA exceeded");
 
 // ------------------------------------------------------------------ format geometry
 __device__ __forceinline__ int epl_of(int fmt) { return fmt == 0 ? 8 : (fmt == 1 ? 16 : 32); }
@@ -61,10 +116,6 @@ __device__ __forceinline__ int xs_index(int k, int epl) {
   int ch = k / per_chunk, r = k % per_chunk;
   int lane = r / epl, e = r % epl;
   return ((ch * (epl / 4) + e / 4) * 32 + lane) * 4 + (e & 3);
-}
-__device__ __forceinline__ void split_range(int n, int parts, int i, int& a, int& b) {
-  a = (int)((long long)n * i / parts);
-  b = (int)((long long)n * (i + 1) / parts);
 }
 __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uint32_t)b << 16); }
 __device__ __forceinline__ float ldg_bf16(const uint16_t* p) { return bf16f(__ldg(p)); }
@@ -99,43 +150,6 @@ struct Xray {
   }
 };
 
-// ------------------------------------------------------------------ per-CTA schedule
-// Both the producer and the consumers derive the same ranges, so they agree on the tile order.
-struct Sched {
-  int q0, q1;    // rows of the virtual q|k|v matrix
-  int o0, o1;    // o_proj output rows
-  int j0, j1;    // FFN units (gate and up rows)
-  int d0, d1;    // down_proj output rows
-  int v0, v1;    // LM-head rows
-  bool unit;     // this CTA runs an attention unit
-  int ug, uc;    // its KV head and chunk
-  int t0, t1;    // positions [t0, t1) of the chunk
-  int ncached;   // positions of the chunk already in the cache (read through the ring)
-  __device__ void make(const KParams& P) {
-    const int G = gridDim.x, b = blockIdx.x;
-    split_range(QKV_ROWS, G, b, q0, q1);
-    split_range(HID, G, b, o0, o1);
-    split_range(FFN, G, b, j0, j1);
-    split_range(HID, G, b, d0, d1);
-    split_range(P.vocab, G, b, v0, v1);
-    unit = b < NKVH * P.units;
-    ug = unit ? b / P.units : 0;
-    uc = unit ? b % P.units : 0;
-    split_range(P.pos + 1, P.units, uc, t0, t1);
-    int c_end = t1 < P.pos ? t1 : P.pos;
-    ncached = unit ? (c_end > t0 ? c_end - t0 : 0) : 0;
-  }
-};
-
-// QKV segment s (0 = q, 1 = k, 2 = v) of the virtual row range.
-__device__ __forceinline__ void qkv_segment(int s, int q0, int q1, int& r0, int& r1, int& base) {
-  const int lo[3] = {0, QROWS, QROWS + KVROWS};
-  const int hi[3] = {QROWS, QROWS + KVROWS, QKV_ROWS};
-  base = lo[s];
-  r0 = max(q0, lo[s]) - lo[s];
-  r1 = min(q1, hi[s]) - lo[s];
-}
-
 // ------------------------------------------------------------------ producer
 struct Producer {
   Smem* s;
@@ -150,9 +164,9 @@ struct Producer {
     slot = n % NSLOT;
     if (n >= NSLOT) {
       uint32_t par = ((n / NSLOT) - 1) & 1;
-      if (!mbar_try_wait(&s->empty[slot], par)) {
+      if (!mbar_test_wait(&s->empty[slot], par)) {
         uint64_t t0 = globaltimer();
-        while (!mbar_try_wait(&s->empty[slot], par)) {
+        while (!mbar_test_wait(&s->empty[slot], par)) {
           if (s->abort) return false;
           if (globaltimer() - t0 > deadline_ns) return false;
         }
@@ -206,7 +220,7 @@ struct Producer {
     for (uint32_t i = first; i < n; ++i) {
       uint32_t slot = i % NSLOT, par = (i / NSLOT) & 1;
       uint64_t t0 = globaltimer();
-      while (!mbar_try_wait(&s->full[slot], par))
+      while (!mbar_test_wait(&s->full[slot], par))
         if (globaltimer() - t0 > 200000000ull) break;
     }
   }
@@ -226,11 +240,7 @@ __device__ void run_producer(const KParams& P, Smem* s, uint8_t* ring) {
   S.make(P);
   for (int l = 0; l < P.n_layers && pr.ok; ++l) {
     const DLayer& L = P.layers[l];
-    for (int sg = 0; sg < 3; ++sg) {
-      int r0, r1, base;
-      qkv_segment(sg, S.q0, S.q1, r0, r1, base);
-      if (r0 < r1) pr.rows(L.m[M_Q + sg], HID, r0, r1);
-    }
+    pr.rows(L.m[M_Q + S.qm], HID, S.qr0, S.qr1);
     if (S.unit) pr.kv(l, S.ug, S.t0, S.ncached);
     pr.rows(L.m[M_O], QROWS, S.o0, S.o1);
     pr.rows(L.m[M_GATE], HID, S.j0, S.j1);
@@ -242,6 +252,15 @@ __device__ void run_producer(const KParams& P, Smem* s, uint8_t* ring) {
 }
 
 // ------------------------------------------------------------------ consumer
+__device__ __forceinline__ void ll_store(llword* p, uint32_t tag, float v) {
+  st_relaxed_u64(p, ((unsigned long long)tag << 32) | (unsigned long long)__float_as_uint(v));
+}
+__device__ __forceinline__ float ll_val(llword w) { return __uint_as_float((uint32_t)(w & 0xFFFFFFFFull)); }
+__device__ __forceinline__ uint32_t ll_tag(llword w) { return (uint32_t)(w >> 32); }
+__device__ __forceinline__ void ld_ll2(const llword* p, llword& a, llword& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+
 template <bool XR>
 struct Consumer {
   Smem* s;
@@ -262,10 +281,18 @@ struct Consumer {
   __device__ __forceinline__ void st(int phase, int kind) {
     if (tid == 0) xr.stamp(phase, kind);
   }
+  __device__ __forceinline__ void mark(int id) {  // sub-phase stamp (kind 4), X-ray builds only
+    if (tid == 0) xr.stamp(id, 4);
+  }
+  __device__ __forceinline__ bool faulted(int phase, int layer) const {
+    return P->fault_cta == (int)blockIdx.x && P->fault_phase == phase && layer == 0;
+  }
+  // Per-thread wait for a ring slot to fill; after an abort it returns at once (the caller keeps
+  // going to the next CTA barrier, where the abort is seen by every warp).
   __device__ void wait_full(uint32_t slot, uint32_t par, int phase, int layer) {
-    if (mbar_try_wait(&s->full[slot], par)) return;
+    if (mbar_test_wait(&s->full[slot], par)) return;
     uint64_t t0 = globaltimer();
-    while (!mbar_try_wait(&s->full[slot], par)) {
+    while (!mbar_test_wait(&s->full[slot], par)) {
       if (s->abort) return;
       if (globaltimer() - t0 > P->timeout_ns) {
         fail(3u, (uint32_t)(phase | (layer << 8) | (blockIdx.x << 16)) | 0x80000000u);
@@ -273,271 +300,559 @@ struct Consumer {
       }
     }
   }
-  // Thread 0 polls `ctr` until it reaches `target`; returns false (CTA-uniformly) on abort.
-  __device__ bool wait_ctr(const uint32_t* ctr, uint32_t target, int phase, int layer) {
-    if (tid == 0) {
-      xr.stamp(phase, 2);
-      if (ld_acquire(ctr) < target) {
-        uint64_t t0 = globaltimer();
-        while (true) {
-          if (ld_acquire(ctr) >= target) break;
-          if (ld_relaxed_u32(&P->sync->status[2]) != 0u) {
-            s->abort = 1;
-            break;
-          }
-          if (globaltimer() - t0 > P->timeout_ns) {
-            fail(3u, (uint32_t)(phase | (layer << 8) | (blockIdx.x << 16)));
-            break;
+  // Wait for the n LL words at src (tag), two per thread per round, and stage them:
+  //  normed: hs[k] = h[k], xs[k] = h[k] * w[k] (w = this thread's two bf16 norm weights of elements
+  //          2 tid, 2 tid + 1, loaded before the wait), and red[warp] = the warp's sum of h^2;
+  //  plain:  xs[k] = x[k].
+  // xs is laid out for a matrix of format fmt. hook() runs before the closing CTA barrier.
+  template <class Hook>
+  __device__ bool poll_stage(const llword* src, int n, uint32_t tag, int phase, int layer, bool normed, uint2 wb,
+                             int fmt, Hook hook) {
+    if (tid == 0) xr.stamp(phase, 2);
+    const int epl = epl_of(fmt);
+    constexpr int MAXW = (FFN + 2 * NCT - 1) / (2 * NCT);  // word pairs per thread, at most
+    const int nw = (n - 2 * tid + 2 * NCT - 1) / (2 * NCT);
+    llword a[MAXW], b[MAXW];
+    // every load of this thread goes out at once; only the late ones are polled again
+#pragma unroll
+    for (int i = 0; i < MAXW; ++i)
+      if (i < nw) ld_ll2(src + 2 * tid + 2 * NCT * i, a[i], b[i]);
+    bool ready = true;
+#pragma unroll
+    for (int i = 0; i < MAXW; ++i)
+      if (i < nw) ready = ready && ll_tag(a[i]) == tag && ll_tag(b[i]) == tag;
+    if (!ready) {
+      const uint64_t t0 = globaltimer();
+      uint32_t it = 0;
+      while (true) {
+        ready = true;
+#pragma unroll
+        for (int i = 0; i < MAXW; ++i) {
+          if (i < nw && (ll_tag(a[i]) != tag || ll_tag(b[i]) != tag)) {
+            ld_ll2(src + 2 * tid + 2 * NCT * i, a[i], b[i]);
+            ready = ready && ll_tag(a[i]) == tag && ll_tag(b[i]) == tag;
           }
         }
+        if (ready) break;
+        if (s->abort) break;
+        if ((++it & 255u) == 0u && P->sync && ld_relaxed_u32(&P->sync->status[2]) != 0u) {
+          s->abort = 1;
+          break;
+        }
+        if (globaltimer() - t0 > P->timeout_ns) {
+          fail(3u, (uint32_t)(phase | (layer << 8) | (blockIdx.x << 16)));
+          break;
+        }
       }
-      xr.stamp(phase, 3);
     }
+    float ss = 0.f;
+#pragma unroll
+    for (int i = 0; i < MAXW; ++i) {
+      if (i >= nw) break;
+      const int k = 2 * tid + 2 * NCT * i;
+      const float va = ll_val(a[i]), vb = ll_val(b[i]);
+      if (normed) {
+        const uint32_t wbits = i == 0 ? wb.x : wb.y;
+        s->hs[k] = va;
+        s->hs[k + 1] = vb;
+        s->xs[xs_index(k, epl)] = va * bf16f((uint16_t)(wbits & 0xFFFFu));
+        s->xs[xs_index(k + 1, epl)] = vb * bf16f((uint16_t)(wbits >> 16));
+        ss = fmaf(va, va, fmaf(vb, vb, ss));
+      } else {
+        s->xs[xs_index(k, epl)] = va;
+        s->xs[xs_index(k + 1, epl)] = vb;
+      }
+    }
+    if (normed) {
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      if (lane == 0) s->red[warp] = ss;
+    }
+    hook();
     bar_consumers(NCT);
+    if (tid == 0) xr.stamp(phase, 3);
     return s->abort == 0;
   }
-  __device__ void signal(uint32_t* ctr, int phase, int layer) {
-    bar_consumers(NCT);
-    if (tid == 0) {
-      bool skip = (P->fault_cta == (int)blockIdx.x) && (P->fault_phase == phase) && layer == 0;
-      if (!skip) red_release_add(ctr, 1u);
+  // Same staging from hs itself (layer 0, whose input is the embedding row already in hs).
+  __device__ void stage_local(uint2 wb, int fmt) {
+    const int epl = epl_of(fmt);
+    float ss = 0.f;
+    for (int k = 2 * tid, it_k = 0; k < HID; k += 2 * NCT, ++it_k) {
+      const uint32_t wbits = it_k == 0 ? wb.x : wb.y;
+      const float va = s->hs[k], vb = s->hs[k + 1];
+      s->xs[xs_index(k, epl)] = va * bf16f((uint16_t)(wbits & 0xFFFFu));
+      s->xs[xs_index(k + 1, epl)] = vb * bf16f((uint16_t)(wbits >> 16));
+      ss = fmaf(va, va, fmaf(vb, vb, ss));
     }
-  }
-
-  // RMSNorm of hs (HID values) with weight w, staged into xs for a matrix of format fmt.
-  __device__ void stage_rmsnorm(const uint16_t* w, int fmt) {
-    float a = s->hs[tid], b = s->hs[tid + NCT];
-    float ss = a * a + b * b;
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) s->red[warp] = ss;
-    bar_consumers(NCT);
-    float tot = 0.f;
+  }
+  // 1 / sqrt(mean(h^2) + eps) from the per-warp sums in red[] (after a CTA barrier).
+  __device__ __forceinline__ float rms_inv() const {
+    float tot = lane < NCW ? s->red[lane] : 0.f;
 #pragma unroll
-    for (int i = 0; i < NCW; ++i) tot += s->red[i];
-    float inv = 1.0f / sqrtf(tot / (float)HID + P->eps);
-    int epl = epl_of(fmt);
-    s->xs[xs_index(tid, epl)] = a * inv * ldg_bf16(w + tid);
-    s->xs[xs_index(tid + NCT, epl)] = b * inv * ldg_bf16(w + tid + NCT);
-    bar_consumers(NCT);
+    for (int o = 8; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    tot = __shfl_sync(0xffffffffu, tot, 0);
+    return 1.0f / sqrtf(tot / (float)HID + P->eps);
   }
-  // Load HID floats written by other CTAs into hs.
-  __device__ void load_h(const float* src) {
-    s->hs[tid] = ld_cg_f32(src + tid);
-    s->hs[tid + NCT] = ld_cg_f32(src + tid + NCT);
-    bar_consumers(NCT);
-  }
-  // Load n floats written by other CTAs straight into the staged layout for format fmt.
+  // Load n floats (plain fp32, e.g. the standalone GEMV input) into the staged layout.
   __device__ void stage_global(const float* src, int n, int fmt) {
     int epl = epl_of(fmt);
-    for (int k = tid; k < n; k += NCT) s->xs[xs_index(k, epl)] = ld_cg_f32(src + k);
+    for (int k = tid; k < n; k += NCT) s->xs[xs_index(k, epl)] = src[k];
     bar_consumers(NCT);
   }
 
-  // Dequant-GEMV over rows [r0, r1) of m (K inputs), streamed through the ring; calls
-  // epi(row, y) on threads 0..rows-in-tile-1 for every finished row. Returns false on abort.
-  template <class Epi>
-  __device__ bool rows(const DMat& m, int K, int r0, int r1, int phase, int layer, Epi epi) {
-    const int fmt = m.fmt, epl = epl_of(fmt), nchunk = K / (32 * epl);
-    const int cb = code_bytes(fmt, K), sbytes = scale_bytes(fmt, K), rpt = tile_rows(fmt, K);
-    for (int r = r0; r < r1; r += rpt) {
-      const int nr = min(rpt, r1 - r);
-      const uint32_t slot = n % NSLOT, par = (n / NSLOT) & 1;
-      wait_full(slot, par, phase, layer);
-      const uint8_t* tile = ring + (size_t)slot * SLOT;
-      const int items = nr * nchunk;
-      const int i0 = warp * items / NCW, i1 = (warp + 1) * items / NCW;
-      float(*part)[NCW] = s->part[n & 1];
-      float acc = 0.f;
-      int cur = -1;
-      for (int i = i0; i < i1; ++i) {
-        const int row = i / nchunk, ch = i - row * nchunk;
-        if (row != cur) {
-          if (cur >= 0) {
+  // Ring protocol at phase granularity: lane i of warp 0 waits for (or releases) tile first + i,
+  // so a phase costs two rounds of mbarrier operations however many rows and warps it has.
+  // wait_tiles must be followed by a CTA barrier before the tiles are read; release_tiles must be
+  // preceded by one after the last read.
+  __device__ __forceinline__ void wait_tiles(int first, int count, int phase, int layer) {
+    if (warp == 0 && lane < count)
+      wait_full((n + first + lane) % NSLOT, ((n + first + lane) / NSLOT) & 1, phase, layer);
+    __syncwarp();
+  }
+  __device__ __forceinline__ void release_tiles(int first, int count) {
+    if (warp == 0 && lane < count) mbar_arrive(&s->empty[(n + first + lane) % NSLOT]);
+  }
+
+  // Lane partial dot products of NR rows against the staged activations.
+  template <int FMT, bool REGX, int NR>
+  __device__ __forceinline__ void dot_rows(const uint8_t* const* code, const uint8_t* const* bsc, int nchunk,
+                                           const float4* xr, float* out) {
+    constexpr int EPL = FMT == 0 ? 8 : (FMT == 1 ? 16 : 32);
+    constexpr int Q = EPL / 4;
+    float acc[NR][2];
 #pragma unroll
-            for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) part[cur][warp] = acc;
-          }
-          acc = 0.f;
-          cur = row;
-        }
-        const uint4 w = *reinterpret_cast<const uint4*>(tile + (size_t)row * cb + ch * 512 + lane * 16);
-        const float4* xv = reinterpret_cast<const float4*>(s->xs) + ch * (epl / 4) * 32 + lane;
-        if (fmt == 0) {
-          float4 x[2] = {xv[0], xv[32]};
-          acc = dot_bf16_16B(w, x, acc);
-        } else if (fmt == 1) {
-          float4 x[4] = {xv[0], xv[32], xv[64], xv[96]};
-          acc = dot_fp8_16B(w, x, acc);
+    for (int r = 0; r < NR; ++r) acc[r][0] = acc[r][1] = 0.f;
+    auto body = [&](int ch, const float4* x) {
+#pragma unroll
+      for (int r = 0; r < NR; ++r) {
+        const uint4 w = *reinterpret_cast<const uint4*>(code[r] + ch * 512 + lane * 16);
+        if constexpr (FMT == 0) {
+          dot_bf16_16B(w, x, acc[r]);
+        } else if constexpr (FMT == 1) {
+          dot_fp8_16B(w, x, acc[r]);
         } else {
-          float4 x[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) x[j] = xv[32 * j];
-          const uint16_t sp = *reinterpret_cast<const uint16_t*>(tile + (size_t)nr * cb + (size_t)row * sbytes +
-                                                                 ch * 64 + lane * 2);
-          const float2 sc = e4m3x2_to_f2(sp);
-          acc = dot_nvfp4_16B(w, x, sc.x, sc.y, acc);
+          const float2 bs = e4m3x2_to_f2(*reinterpret_cast<const uint16_t*>(bsc[r] + ch * 64 + lane * 2));
+          dot_nvfp4_16B(w, x, bs.x, bs.y, acc[r]);
         }
       }
-      if (cur >= 0) {
+    };
+    if constexpr (REGX) {
+      constexpr int NCH = 1024 / (32 * EPL);
 #pragma unroll
-        for (int o = 16; o; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) part[cur][warp] = acc;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s->empty[slot]);
-      ++n;
-      bar_consumers(NCT);
-      if (s->abort) return false;
-      if (tid < nr) {
-        const int row = tid;
-        float y = 0.f;
-        for (int w = 0; w < NCW; ++w) {
-          const int a = w * items / NCW, b = (w + 1) * items / NCW;
-          if (a < b && a < (row + 1) * nchunk && b > row * nchunk) y += part[row][w];
-        }
-        if (fmt == 1) y *= __ldg(reinterpret_cast<const float*>(m.scale) + r + row);
-        else if (fmt == 2) y *= m.tscale;
-        epi(r + row, y);
+      for (int ch = 0; ch < NCH; ++ch) body(ch, &xr[ch * Q]);
+    } else {
+      const float4* xs4 = reinterpret_cast<const float4*>(s->xs) + lane;
+      for (int ch = 0; ch < nchunk; ++ch) {
+        float4 x[Q];
+#pragma unroll
+        for (int j = 0; j < Q; ++j) x[j] = xs4[32 * (ch * Q + j)];
+        body(ch, x);
       }
     }
-    return true;
+#pragma unroll
+    for (int r = 0; r < NR; ++r) out[r] = acc[r][0] + acc[r][1];
+  }
+
+  // Epilogue of a GEMV phase, chosen at run time (one code copy per format instead of one per
+  // phase keeps the kernel small).
+  enum EpiKind { EPI_QKV, EPI_RESID, EPI_HEAD, EPI_OUT, EPI_ACT };
+  struct EpiCtx {
+    int kind;
+    uint32_t tag;
+    bool skip;    // test hook: drop the outputs
+    float inv;    // RMSNorm factor of the input (applied to y), 1 otherwise
+    llword* ll;   // LL output base (row index added)
+    float* fout;  // fp32 output (logits, standalone GEMV)
+    float* dbg;   // residual debug row
+  };
+  float best;
+  int besti;
+  __device__ __forceinline__ void epi_row(const EpiCtx& e, int r, float y) {
+    if (e.kind == EPI_QKV) {
+      if (!e.skip) ll_store(e.ll + r, e.tag, y * e.inv);
+    } else if (e.kind == EPI_RESID) {
+      const float v = s->hs[r] + y;
+      if (!e.skip) ll_store(e.ll + r, e.tag, v);
+      if (e.dbg) e.dbg[r] = v;
+    } else if (e.kind == EPI_HEAD) {
+      y *= e.inv;
+      if (e.fout) e.fout[r] = y;
+      if (y > best || (y == best && r < besti)) {
+        best = y;
+        besti = r;
+      }
+    } else {
+      e.fout[r] = y;
+    }
+  }
+
+  // ---------------------------------------------------------------- dequant-GEMV engine
+  // One phase = rows [r0, r1) of matrix a (and, PAIRED, the same rows of matrix b: gate with up),
+  // streamed by the producer as tiles of `rpt` rows (a's tiles, then b's). Warp w computes rows
+  // w + k NCW, four at a time (four independent dot products; PAIRED: units u and u + NCW, each
+  // with its gate and up row). Every warp waits for and releases every tile of the phase exactly
+  // once, in order per matrix. srow: FP8 row scales staged in shared memory (a's rows, then b's).
+  template <int FMT, bool REGX, bool PAIRED, int NR>
+  __device__ void gemv_t(const DMat& ma, const DMat& mb, int r0, int r1, int K, const float* srow, const EpiCtx& e) {
+    constexpr int EPL = FMT == 0 ? 8 : (FMT == 1 ? 16 : 32);
+    const int nchunk = K / (32 * EPL);
+    const int cb = code_bytes(FMT, K), sbytes = scale_bytes(FMT, K), rpt = tile_rows(FMT, K);
+    const uint32_t rmag = 0xFFFFFFFFu / (uint32_t)rpt + 1u;  // i / rpt == umulhi(i, rmag) for i < 2^27
+    const int nrows = r1 - r0;
+    const int T = (nrows + rpt - 1) / rpt;  // tiles of one matrix
+    const int ntiles = PAIRED ? 2 * T : T;
+    float4 xr[8];
+    if constexpr (REGX) {
+      const float4* xs4 = reinterpret_cast<const float4*>(s->xs) + lane;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) xr[q] = xs4[32 * q];
+    }
+    const float* sca = reinterpret_cast<const float*>(ma.scale) + r0;
+    const float* scb = reinterpret_cast<const float*>(mb.scale) + r0;
+    constexpr int UPP = PAIRED ? 2 : NR;  // units (rows of a) per pass
+    // batches of tiles: PAIRED phases take all 2T tiles at once (they fit the ring); others take
+    // up to 5, so a long phase (the LM head) keeps the producer streaming while it computes
+    const int tpb = PAIRED ? T : (T < 5 ? T : 5);
+    for (int bt = 0; bt < T; bt += tpb) {
+      const int nb = min(tpb, T - bt);
+      wait_tiles(bt, nb, PH_WAIT, -1);
+      if (PAIRED) wait_tiles(T + bt, nb, PH_WAIT, -1);
+      bar_consumers(NCT);
+      const int row_end = min((bt + nb) * rpt, nrows);
+      for (int base = bt * rpt + warp; base < row_end; base += UPP * NCW) {
+        int ridx[NR];
+        bool valid[NR];
+        const uint8_t* code[NR];
+        const uint8_t* bsc[NR];
+        float sc[NR];
+#pragma unroll
+        for (int k = 0; k < NR; ++k) {
+          const int u = base + (PAIRED ? (k >> 1) : k) * NCW;  // row of a (or unit)
+          const bool isb = PAIRED && (k & 1);
+          valid[k] = u < row_end;
+          const int uu = valid[k] ? u : base;
+          const int tl = (int)__umulhi((uint32_t)uu, rmag);
+          const int rit = uu - tl * rpt;
+          const int nr = tl == T - 1 ? nrows - tl * rpt : rpt;
+          const int tt = isb ? T + tl : tl;
+          ridx[k] = uu;
+          const uint8_t* tile = ring + (size_t)((n + tt) % NSLOT) * SLOT;
+          code[k] = tile + (size_t)rit * cb;
+          bsc[k] = tile + (size_t)nr * cb + (size_t)rit * sbytes;
+          if constexpr (FMT == 1) {
+            const int si = isb ? nrows + uu : uu;
+            sc[k] = srow ? srow[si] : __ldg((isb ? scb : sca) + uu);
+          } else {
+            sc[k] = FMT == 2 ? (isb ? mb.tscale : ma.tscale) : 1.f;
+          }
+        }
+        float part[NR];
+        dot_rows<FMT, REGX, NR>(code, bsc, nchunk, xr, part);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+#pragma unroll
+          for (int k = 0; k < NR; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k], o);
+        }
+        if (lane == 0) {
+          if constexpr (PAIRED) {
+#pragma unroll
+            for (int k = 0; k < NR; k += 2) {
+              if (valid[k]) {
+                const float g = part[k] * sc[k] * e.inv, up = part[k + 1] * sc[k + 1] * e.inv;
+                if (!e.skip) ll_store(e.ll + ridx[k], e.tag, g / (1.0f + expf(-g)) * up);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < NR; ++k)
+              if (valid[k]) epi_row(e, r0 + ridx[k], part[k] * sc[k]);
+          }
+        }
+      }
+      bar_consumers(NCT);  // every read of the batch is done
+      release_tiles(bt, nb);
+      if (PAIRED) release_tiles(T + bt, nb);
+    }
+    n += ntiles;
+  }
+  // Dispatch on format and width (the one call site of the engine).
+  __device__ void gemv(bool paired, const DMat& ma, const DMat& mb, int r0, int r1, int K, const float* srow,
+                       const EpiCtx& e) {
+    if (r0 >= r1) return;
+    const int fmt = ma.fmt;
+    const bool one = r1 - r0 <= NCW;  // at most one row per warp: one row per pass
+    if (paired) {
+      if (fmt == 0) gemv_t<0, true, true, 4>(ma, mb, r0, r1, K, srow, e);
+      else if (fmt == 1) gemv_t<1, true, true, 4>(ma, mb, r0, r1, K, srow, e);
+      else gemv_t<2, true, true, 4>(ma, mb, r0, r1, K, srow, e);
+    } else if (K == 1024) {
+      if (fmt == 0) gemv_t<0, true, false, 4>(ma, mb, r0, r1, K, srow, e);
+      else if (fmt == 1) gemv_t<1, true, false, 4>(ma, mb, r0, r1, K, srow, e);
+      else gemv_t<2, true, false, 4>(ma, mb, r0, r1, K, srow, e);
+    } else if (one) {
+      if (fmt == 0) gemv_t<0, false, false, 1>(ma, mb, r0, r1, K, srow, e);
+      else if (fmt == 1) gemv_t<1, false, false, 1>(ma, mb, r0, r1, K, srow, e);
+      else gemv_t<2, false, false, 1>(ma, mb, r0, r1, K, srow, e);
+    } else {
+      if (fmt == 0) gemv_t<0, false, false, 4>(ma, mb, r0, r1, K, srow, e);
+      else if (fmt == 1) gemv_t<1, false, false, 4>(ma, mb, r0, r1, K, srow, e);
+      else gemv_t<2, false, false, 4>(ma, mb, r0, r1, K, srow, e);
+    }
   }
 
   // One attention unit: KV head g, positions [S.t0, S.t1) of layer l.
-  __device__ bool attention(const Sched& S, const DLayer& L, int l) {
+  __device__ bool attention(const Sched& S, const DLayer& L, int l, uint32_t tag) {
     const KParams& p = *P;
     const int g = S.ug;
-    // raw q (two heads), k, v of KV head g
-    float val;
-    if (tid < 2 * HD) val = ld_cg_f32(p.qkv + GQA * HD * g + tid);
-    else if (tid < 3 * HD) val = ld_cg_f32(p.qkv + QROWS + HD * g + (tid - 2 * HD));
-    else val = ld_cg_f32(p.qkv + QROWS + KVROWS + HD * g + (tid - 3 * HD));
-    float ss = val * val;
+    // Warps 0..3 own one 128-wide vector each (q of head 2g, q of head 2g+1, k, v); lane holds
+    // elements lane + 32 j, so RoPE pairs (i, i + 64) stay in one lane and QK-norm is a shuffle.
+    if (warp < 4) {
+      const int src = warp < 2 ? GQA * HD * g + warp * HD : (warp == 2 ? QROWS + HD * g : QROWS + KVROWS + HD * g);
+      // loads that do not depend on this step's data go out before the wait
+      float nw[4] = {1.f, 1.f, 1.f, 1.f}, rc[2], rsn[2];
+      if (warp < 3) {
+        const uint16_t* w = warp < 2 ? L.q_norm : L.k_norm;
 #pragma unroll
-    for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    if (lane == 0) s->red[warp] = ss;
-    bar_consumers(NCT);
-    const int vec = warp / 4, d = tid & (HD - 1);
-    float nv = val;
-    if (vec < 3) {  // QK-norm: RMSNorm over the head
-      float tot = s->red[4 * vec] + s->red[4 * vec + 1] + s->red[4 * vec + 2] + s->red[4 * vec + 3];
-      float inv = 1.0f / sqrtf(tot / (float)HD + p.eps);
-      nv = val * inv * ldg_bf16((vec < 2 ? L.q_norm : L.k_norm) + d);
-    }
-    float* dst = vec == 0 ? s->qs[0] : (vec == 1 ? s->qs[1] : (vec == 2 ? s->kn : s->vn));
-    dst[d] = nv;
-    bar_consumers(NCT);
-    if (tid < 3 * (HD / 2)) {  // RoPE, half-split pairs (i, i + 64)
-      const int which = tid / (HD / 2), i = tid % (HD / 2);
-      float* x = which == 0 ? s->qs[0] : (which == 1 ? s->qs[1] : s->kn);
-      const float c = __ldg(p.rope_cos + (size_t)p.pos * (HD / 2) + i);
-      const float sn = __ldg(p.rope_sin + (size_t)p.pos * (HD / 2) + i);
-      const float a = x[i], b = x[i + HD / 2];
-      x[i] = a * c - b * sn;
-      x[i + HD / 2] = b * c + a * sn;
-    }
-    bar_consumers(NCT);
-    if (tid < 2 * HD) {  // the cache holds bf16: round the new key and value
-      const int which = tid / HD, dd = tid % HD;
-      float* x = which ? s->vn : s->kn;
-      const __nv_bfloat16 hb = __float2bfloat16_rn(x[dd]);
-      const uint16_t bits = __bfloat16_as_ushort(hb);
-      x[dd] = bf16f(bits);
-      if (S.uc == p.units - 1) {
-        uint16_t* cache = which ? p.vc : p.kc;
-        cache[(((size_t)l * NKVH + g) * p.max_ctx + p.pos) * HD + dd] = bits;
+        for (int j = 0; j < 4; ++j) nw[j] = ldg_bf16(w + lane + 32 * j);
       }
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        rc[j] = __ldg(p.rope_cos + (size_t)p.pos * (HD / 2) + lane + 32 * j);
+        rsn[j] = __ldg(p.rope_sin + (size_t)p.pos * (HD / 2) + lane + 32 * j);
+      }
+      if (lane == 0 && warp == 0) xr.stamp(PH_QKV, 2);
+      float v[4];
+      {
+        llword wv[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wv[j] = ld_relaxed_u64(p.qkv + src + lane + 32 * j);
+        bool ready = ll_tag(wv[0]) == tag && ll_tag(wv[1]) == tag && ll_tag(wv[2]) == tag && ll_tag(wv[3]) == tag;
+        if (!ready) {
+          const uint64_t t0 = globaltimer();
+          uint32_t it = 0;
+          while (true) {
+            ready = true;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              if (ll_tag(wv[j]) != tag) {
+                wv[j] = ld_relaxed_u64(p.qkv + src + lane + 32 * j);
+                ready = ready && ll_tag(wv[j]) == tag;
+              }
+            }
+            if (ready || s->abort) break;
+            if ((++it & 255u) == 0u && ld_relaxed_u32(&p.sync->status[2]) != 0u) {
+              s->abort = 1;
+              break;
+            }
+            if (globaltimer() - t0 > p.timeout_ns) {
+              fail(3u, (uint32_t)(PH_QKV | (l << 8) | (blockIdx.x << 16)));
+              break;
+            }
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = ll_val(wv[j]);
+      }
+      if (warp < 3) {  // QK-norm (RMSNorm over the head), then RoPE at pos
+        float ss = v[0] * v[0] + v[1] * v[1] + v[2] * v[2] + v[3] * v[3];
+#pragma unroll
+        for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float inv = 1.0f / sqrtf(ss / (float)HD + p.eps);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = v[j] * inv * nw[j];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float a = v[j], b = v[j + 2];
+          v[j] = a * rc[j] - b * rsn[j];
+          v[j + 2] = b * rc[j] + a * rsn[j];
+        }
+      }
+      if (warp >= 2) {  // the cache holds bf16: round the new key and value
+        uint16_t* cache = warp == 2 ? p.kc : p.vc;
+        const size_t row = (((size_t)l * NKVH + g) * p.max_ctx + p.pos) * HD;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
+          v[j] = bf16f(bits);
+          if (S.uc == p.units - 1) cache[row + lane + 32 * j] = bits;
+        }
+      }
+      float* dst = warp == 0 ? s->qs[0] : (warp == 1 ? s->qs[1] : (warp == 2 ? s->kn : s->vn));
+#pragma unroll
+      for (int j = 0; j < 4; ++j) dst[lane + 32 * j] = v[j];
+      if (lane == 0 && warp == 0) xr.stamp(PH_QKV, 3);
     }
-    bar_consumers(NCT);
-    // scores
     const int np = S.t1 - S.t0, ntiles = (S.ncached + KVT - 1) / KVT;
-    for (int i = 0; i < ntiles; ++i) wait_full((n + i) % NSLOT, ((n + i) / NSLOT) & 1, PH_ATTN, l);
+    wait_tiles(0, ntiles, PH_ATTN, l);
     bar_consumers(NCT);
+    mark(30);
     if (s->abort) return false;
     const float scale = 0.08838834764831845f;  // 1/sqrt(128)
-    float q0[4], q1[4];
+    // ---- scores: a group of 8 lanes per position, 16 dims per lane, both heads at once
+    {
+      const int grp = lane >> 3, gl = lane & 7;
+      float q0[16], q1[16];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      q0[e] = s->qs[0][4 * lane + e];
-      q1[e] = s->qs[1][4 * lane + e];
-    }
-    for (int t = warp; t < np; t += NCW) {
-      float k4[4];
-      if (t < S.ncached) {
-        const uint8_t* tile = ring + (size_t)((n + t / KVT) % NSLOT) * SLOT;
-        const uint2 raw = *reinterpret_cast<const uint2*>(tile + (t % KVT) * HD * 2 + lane * 8);
-        k4[0] = __uint_as_float(raw.x << 16);
-        k4[1] = __uint_as_float(raw.x & 0xFFFF0000u);
-        k4[2] = __uint_as_float(raw.y << 16);
-        k4[3] = __uint_as_float(raw.y & 0xFFFF0000u);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) k4[e] = s->kn[4 * lane + e];
+      for (int e = 0; e < 8; ++e) {
+        q0[e] = s->qs[0][8 * gl + e];
+        q1[e] = s->qs[1][8 * gl + e];
+        q0[8 + e] = s->qs[0][64 + 8 * gl + e];
+        q1[8 + e] = s->qs[1][64 + 8 * gl + e];
       }
-      float a = 0.f, b = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY;
+      for (int t = warp * 4 + grp; t - grp < np; t += NCW * 4) {
+        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+        if (t < np) {
+          uint4 k0, k1;
+          if (t < S.ncached) {
+            const uint8_t* row = ring + (size_t)((n + t / KVT) % NSLOT) * SLOT + (t % KVT) * HD * 2;
+            k0 = *reinterpret_cast<const uint4*>(row + gl * 16);
+            k1 = *reinterpret_cast<const uint4*>(row + 128 + gl * 16);
+          } else {
+            // the new position: convert the float key to the packed bf16 layout on the fly
+            const float* kr = s->kn;
+            uint32_t w[8];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        a = fmaf(q0[e], k4[e], a);
-        b = fmaf(q1[e], k4[e], b);
+            for (int e = 0; e < 4; ++e) {
+              w[e] = (__float_as_uint(kr[8 * gl + 2 * e]) >> 16) | (__float_as_uint(kr[8 * gl + 2 * e + 1]) & 0xFFFF0000u);
+              w[4 + e] = (__float_as_uint(kr[64 + 8 * gl + 2 * e]) >> 16) |
+                         (__float_as_uint(kr[64 + 8 * gl + 2 * e + 1]) & 0xFFFF0000u);
+            }
+            k0 = make_uint4(w[0], w[1], w[2], w[3]);
+            k1 = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float lo = __uint_as_float(kw[e] << 16), hi = __uint_as_float(kw[e] & 0xFFFF0000u);
+            a0 = fmaf(q0[2 * e], lo, a0);
+            a1 = fmaf(q0[2 * e + 1], hi, a1);
+            b0 = fmaf(q1[2 * e], lo, b0);
+            b1 = fmaf(q1[2 * e + 1], hi, b1);
+          }
+        }
+        float a = a0 + a1, b = b0 + b1;
+#pragma unroll
+        for (int o = 4; o; o >>= 1) {
+          a += __shfl_xor_sync(0xffffffffu, a, o);
+          b += __shfl_xor_sync(0xffffffffu, b, o);
+        }
+        if (t < np) {
+          a *= scale;
+          b *= scale;
+          if (gl == 0) {
+            s->sc[0][t] = a;
+            s->sc[1][t] = b;
+          }
+          m0 = fmaxf(m0, a);
+          m1 = fmaxf(m1, b);
+        }
       }
 #pragma unroll
       for (int o = 16; o; o >>= 1) {
-        a += __shfl_xor_sync(0xffffffffu, a, o);
-        b += __shfl_xor_sync(0xffffffffu, b, o);
+        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
       }
       if (lane == 0) {
-        s->sc[0][t] = a * scale;
-        s->sc[1][t] = b * scale;
+        s->red[warp] = m0;
+        s->red[NCW + warp] = m1;
       }
     }
     bar_consumers(NCT);
-    if (warp < 2) {  // softmax numerators and partial sums of this chunk
-      float m = -INFINITY;
-      for (int t = lane; t < np; t += 32) m = fmaxf(m, s->sc[warp][t]);
-#pragma unroll
-      for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      float sum = 0.f;
-      for (int t = lane; t < np; t += 32) {
-        const float e = expf(s->sc[warp][t] - m);
-        s->sc[warp][t] = e;
-        sum += e;
-      }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-      if (lane == 0) {
-        s->stat[warp] = m;
-        s->stat[2 + warp] = sum;
-      }
-    }
-    bar_consumers(NCT);
+    mark(33);
+    // ---- softmax numerators of this chunk and their per-head sums
     {
-      const int h = tid >> 8, dd = (tid & 255) >> 1, half = tid & 1;
-      float acc = 0.f;
-      for (int t = half; t < np; t += 2) {
-        float vv;
-        if (t < S.ncached) {
-          const uint8_t* tile = ring + (size_t)((n + t / KVT) % NSLOT) * SLOT;
-          vv = bf16f(*reinterpret_cast<const uint16_t*>(tile + SLOT / 2 + (t % KVT) * HD * 2 + dd * 2));
-        } else {
-          vv = s->vn[dd];
-        }
-        acc = fmaf(s->sc[h][t], vv, acc);
+      float M0 = lane < NCW ? s->red[lane] : -INFINITY, M1 = lane < NCW ? s->red[NCW + lane] : -INFINITY;
+#pragma unroll
+      for (int o = 8; o; o >>= 1) {
+        M0 = fmaxf(M0, __shfl_xor_sync(0xffffffffu, M0, o));
+        M1 = fmaxf(M1, __shfl_xor_sync(0xffffffffu, M1, o));
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      if (half == 0) {
-        float* part = p.attp + (((size_t)g * MAXC + S.uc) * 2 + h) * PART_STRIDE;
-        part[4 + dd] = acc;
-        if (dd == 0) {
-          part[0] = s->stat[h];
-          part[1] = s->stat[2 + h];
-        }
+      M0 = __shfl_sync(0xffffffffu, M0, 0);
+      M1 = __shfl_sync(0xffffffffu, M1, 0);
+      float l0 = 0.f, l1 = 0.f;
+      for (int i = tid; i < 2 * np; i += NCT) {
+        const int h = i >= np, t = h ? i - np : i;
+        const float e = expf(s->sc[h][t] - (h ? M1 : M0));
+        s->sc[h][t] = e;
+        if (h) l1 += e;
+        else l0 += e;
+      }
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      }
+      if (lane == 0) {
+        s->red[2 * NCW + warp] = l0;
+        s->red[3 * NCW + warp] = l1;
+      }
+      if (tid == 0) {
+        s->stat[0] = M0;
+        s->stat[1] = M1;
       }
     }
     bar_consumers(NCT);
-    for (int i = 0; i < ntiles; ++i)
-      if (lane == 0) mbar_arrive(&s->empty[(n + i) % NSLOT]);
+    mark(34);
+    // ---- weighted sum of V: work item (slice, d), positions t = slice (mod 4), both heads
+    for (int wi = tid; wi < 4 * HD; wi += NCT) {
+      const int d = wi & (HD - 1), slice = wi >> 7;
+      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
+      auto vat = [&](int t) {
+        const uint8_t* tile = ring + (size_t)((n + t / KVT) % NSLOT) * SLOT;
+        return bf16f(*reinterpret_cast<const uint16_t*>(tile + SLOT / 2 + (t % KVT) * HD * 2 + d * 2));
+      };
+      int t = slice;
+      for (; t + 4 < S.ncached; t += 8) {  // two positions per iteration, independent chains
+        const float v0 = vat(t), v1 = vat(t + 4);
+        a00 = fmaf(s->sc[0][t], v0, a00);
+        a10 = fmaf(s->sc[1][t], v0, a10);
+        a01 = fmaf(s->sc[0][t + 4], v1, a01);
+        a11 = fmaf(s->sc[1][t + 4], v1, a11);
+      }
+      for (; t < S.ncached; t += 4) {
+        const float v0 = vat(t);
+        a00 = fmaf(s->sc[0][t], v0, a00);
+        a10 = fmaf(s->sc[1][t], v0, a10);
+      }
+      if (np > S.ncached && ((np - 1) & 3) == slice) {  // the new position (held in vn)
+        const float v0 = s->vn[d];
+        a01 = fmaf(s->sc[0][np - 1], v0, a01);
+        a11 = fmaf(s->sc[1][np - 1], v0, a11);
+      }
+      float* xsum = s->xs;  // free during attention
+      xsum[(slice * 2 + 0) * HD + d] = a00 + a01;
+      xsum[(slice * 2 + 1) * HD + d] = a10 + a11;
+    }
+    bar_consumers(NCT);
+    mark(35);
+    release_tiles(0, ntiles);
     n += ntiles;
+    if (tid < 2 * HD) {
+      const int h = tid / HD, d = tid % HD;
+      const float* xsum = s->xs;
+      const float acc = (xsum[(0 * 2 + h) * HD + d] + xsum[(1 * 2 + h) * HD + d]) +
+                        (xsum[(2 * 2 + h) * HD + d] + xsum[(3 * 2 + h) * HD + d]);
+      float lsum = lane < NCW ? s->red[(2 + h) * NCW + lane] : 0.f;
+#pragma unroll
+      for (int o = 8; o; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
+      lsum = __shfl_sync(0xffffffffu, lsum, 0);
+      if (p.units == 1) {  // one unit covers the whole context: no merge needed
+        if (!faulted(PH_ATTN, l)) ll_store(p.att + GQA * HD * g + tid, tag, acc / lsum);
+      } else {
+        float* part = p.attp + (((size_t)g * MAXC + S.uc) * 2 + h) * PART_STRIDE;
+        part[4 + d] = acc;
+        if (d == 0) {
+          part[0] = s->stat[h];
+          part[1] = lsum;
+        }
+      }
+    }
+    if (p.units == 1) return true;
+    bar_consumers(NCT);
     // the last unit of this KV head to finish merges the chunks
     if (tid == 0) {
       fence_acqrel_gpu();
@@ -545,30 +860,27 @@ struct Consumer {
       s->flag = (old == (uint32_t)((l + 1) * p.units - 1)) ? 1 : 0;
     }
     bar_consumers(NCT);
-    if (s->flag) {
-      if (tid < 2 * HD) {
-        const int h = tid / HD, dd = tid % HD;
-        float M = -INFINITY;
-        for (int c = 0; c < p.units; ++c)
-          M = fmaxf(M, ld_cg_f32(p.attp + (((size_t)g * MAXC + c) * 2 + h) * PART_STRIDE));
-        float Lsum = 0.f, o = 0.f;
-        for (int c = 0; c < p.units; ++c) {
-          const float* part = p.attp + (((size_t)g * MAXC + c) * 2 + h) * PART_STRIDE;
-          const float w = expf(ld_cg_f32(part) - M);
-          Lsum = fmaf(w, ld_cg_f32(part + 1), Lsum);
-          o = fmaf(w, ld_cg_f32(part + 4 + dd), o);
-        }
-        p.att[GQA * HD * g + tid] = o / Lsum;
+    if (s->flag && tid < 2 * HD && !faulted(PH_ATTN, l)) {
+      const int h = tid / HD, dd = tid % HD;
+      float M = -INFINITY;
+      for (int c = 0; c < p.units; ++c)
+        M = fmaxf(M, ld_cg_f32(p.attp + (((size_t)g * MAXC + c) * 2 + h) * PART_STRIDE));
+      float Lsum = 0.f, o = 0.f;
+      for (int c = 0; c < p.units; ++c) {
+        const float* part = p.attp + (((size_t)g * MAXC + c) * 2 + h) * PART_STRIDE;
+        const float w = expf(ld_cg_f32(part) - M);
+        Lsum = fmaf(w, ld_cg_f32(part + 1), Lsum);
+        o = fmaf(w, ld_cg_f32(part + 4 + dd), o);
       }
-      signal(&p.sync->c[PH_ATTN][0], PH_ATTN, l);
+      ll_store(p.att + GQA * HD * g + tid, tag, o / Lsum);
     }
     return true;
   }
 
   __device__ void run(const KParams& p) {
     const int G = gridDim.x;
-    Sched S;
-    S.make(p);
+    if (tid == 0) s->sched.make(p);  // published by the barrier after the embedding
+    const Sched& S = s->sched;
     // ---------------- embedding: h = row `token` of the tied matrix (every CTA, no wait)
     st(PH_EMBED, 0);
     const int token = p.token_ptr ? *(volatile const int32_t*)p.token_ptr : p.token;
@@ -576,6 +888,12 @@ struct Consumer {
       if (tid == 0) fail(4u, (uint32_t)blockIdx.x << 16);
       bar_consumers(NCT);
       return;
+    }
+    {
+      const uint32_t* src = reinterpret_cast<const uint32_t*>(p.layers);
+      uint32_t* dst = reinterpret_cast<uint32_t*>(s->lay);
+      const int nw = p.n_layers * (int)(sizeof(DLayer) / 4);
+      for (int i = tid; i < nw; i += NCT) dst[i] = __ldg(src + i);
     }
     {
       const DMat& E = p.embed;
@@ -594,112 +912,113 @@ struct Consumer {
     }
     bar_consumers(NCT);
     st(PH_EMBED, 1);
-    for (int l = 0; l < p.n_layers; ++l) {
-      const DLayer& L = p.layers[l];
-      // ---------------- QKV
-      if (l > 0) {
-        if (!wait_ctr(&p.sync->c[PH_DOWN][0], (uint32_t)(l * G), PH_DOWN, l)) return;
-        load_h(p.h_mlp);
-      }
-      st(PH_QKV, 0);
-      stage_rmsnorm(L.ln_in, L.m[M_Q].fmt);
-      for (int sg = 0; sg < 3; ++sg) {
-        int r0, r1, base;
-        qkv_segment(sg, S.q0, S.q1, r0, r1, base);
-        if (r0 >= r1) continue;
-        float* out = p.qkv + base;
-        if (!rows(L.m[M_Q + sg], HID, r0, r1, PH_QKV, l, [&](int r, float y) { out[r] = y; })) return;
-      }
-      signal(&p.sync->c[PH_QKV][0], PH_QKV, l);
-      st(PH_QKV, 1);
-      // ---------------- attention
-      if (S.unit) {
-        if (!wait_ctr(&p.sync->c[PH_QKV][0], (uint32_t)((l + 1) * G), PH_QKV, l)) return;
-        st(PH_ATTN, 0);
-        if (!attention(S, L, l)) return;
-        st(PH_ATTN, 1);
-      }
-      // ---------------- o_proj + residual
-      if (!wait_ctr(&p.sync->c[PH_ATTN][0], (uint32_t)((l + 1) * NKVH), PH_ATTN, l)) return;
-      st(PH_O, 0);
-      stage_global(p.att, QROWS, L.m[M_O].fmt);
-      {
-        float* hout = p.h_attn;
-        const float* hin = s->hs;
-        if (!rows(L.m[M_O], QROWS, S.o0, S.o1, PH_O, l, [&](int r, float y) { hout[r] = hin[r] + y; })) return;
-      }
-      signal(&p.sync->c[PH_O][0], PH_O, l);
-      st(PH_O, 1);
-      // ---------------- post-attention RMSNorm + gate/up + SwiGLU
-      if (!wait_ctr(&p.sync->c[PH_O][0], (uint32_t)((l + 1) * G), PH_O, l)) return;
-      st(PH_GATEUP, 0);
-      load_h(p.h_attn);
-      stage_rmsnorm(L.ln_post, L.m[M_GATE].fmt);
-      {
-        float* gs = s->gs;
-        float* us = s->us;
-        const int j0 = S.j0;
-        if (!rows(L.m[M_GATE], HID, S.j0, S.j1, PH_GATEUP, l, [&](int r, float y) { gs[r - j0] = y; })) return;
-        if (!rows(L.m[M_UP], HID, S.j0, S.j1, PH_GATEUP, l, [&](int r, float y) { us[r - j0] = y; })) return;
-      }
-      bar_consumers(NCT);
-      if (tid < S.j1 - S.j0) {
-        const float gv = s->gs[tid];
-        p.act[S.j0 + tid] = gv / (1.0f + expf(-gv)) * s->us[tid];
-      }
-      signal(&p.sync->c[PH_GATEUP][0], PH_GATEUP, l);
-      st(PH_GATEUP, 1);
-      // ---------------- down_proj + residual
-      if (!wait_ctr(&p.sync->c[PH_GATEUP][0], (uint32_t)((l + 1) * G), PH_GATEUP, l)) return;
-      st(PH_DOWN, 0);
-      stage_global(p.act, FFN, L.m[M_DOWN].fmt);
-      {
-        float* hout = p.h_mlp;
-        const float* hin = s->hs;
-        float* dbg = p.hidden_dbg ? p.hidden_dbg + (size_t)(l + 1) * HID : nullptr;
-        if (!rows(L.m[M_DOWN], FFN, S.d0, S.d1, PH_DOWN, l, [&](int r, float y) {
-              const float v = hin[r] + y;
-              hout[r] = v;
-              if (dbg) dbg[r] = v;
-            }))
+    float* rs = s->rs;
+    best = -INFINITY;
+    besti = 0x7FFFFFFF;
+    // One pass per (layer, step); the single GEMV and wait call sites keep one code copy each.
+    enum { ST_QKV = 0, ST_ATTN, ST_O, ST_GU, ST_DOWN, ST_HEAD };
+    for (int l = 0; l <= p.n_layers; ++l) {
+      const bool head = l == p.n_layers;
+      const DLayer& L = s->lay[head ? 0 : l];
+      const uint32_t tag = p.tagbase + (uint32_t)l;
+      for (int step = head ? ST_HEAD : ST_QKV; step <= (head ? ST_HEAD : ST_DOWN); ++step) {
+        if (step == ST_ATTN) {
+          if (S.unit) {
+            st(PH_ATTN, 0);
+            if (!attention(S, L, l, tag)) return;
+            st(PH_ATTN, 1);
+          }
+          continue;
+        }
+        // ---- describe the phase
+        DMat ma, mb;
+        int r0, r1, K, phase;
+        bool paired = false, normed;
+        const llword* src;
+        int nsrc;
+        uint32_t stag;
+        const uint16_t* nw = nullptr;
+        EpiCtx e;
+        e.tag = tag;
+        e.inv = 1.f;
+        e.fout = nullptr;
+        e.dbg = nullptr;
+        if (step == ST_QKV) {
+          ma = L.m[M_Q + S.qm], r0 = S.qr0, r1 = S.qr1;
+          K = HID, phase = PH_QKV, normed = true;
+          src = p.h_mlp, nsrc = HID, stag = tag - 1, nw = L.ln_in;
+          e.kind = EPI_QKV, e.ll = p.qkv + S.qbase, e.skip = faulted(PH_QKV, l);
+        } else if (step == ST_O) {
+          ma = L.m[M_O], r0 = S.o0, r1 = S.o1;
+          K = QROWS, phase = PH_O, normed = false;
+          src = p.att, nsrc = QROWS, stag = tag;
+          e.kind = EPI_RESID, e.ll = p.h_attn, e.skip = faulted(PH_O, l);
+        } else if (step == ST_GU) {
+          ma = L.m[M_GATE], mb = L.m[M_UP], r0 = S.j0, r1 = S.j1;
+          K = HID, phase = PH_GATEUP, normed = true, paired = true;
+          src = p.h_attn, nsrc = HID, stag = tag, nw = L.ln_post;
+          e.kind = EPI_ACT, e.ll = p.act + S.j0, e.skip = faulted(PH_GATEUP, l);
+        } else if (step == ST_DOWN) {
+          ma = L.m[M_DOWN], r0 = S.d0, r1 = S.d1;
+          K = FFN, phase = PH_DOWN, normed = false;
+          src = p.act, nsrc = FFN, stag = tag;
+          e.kind = EPI_RESID, e.ll = p.h_mlp, e.skip = faulted(PH_DOWN, l);
+          e.dbg = p.hidden_dbg ? p.hidden_dbg + (size_t)(l + 1) * HID : nullptr;
+        } else {  // final RMSNorm + LM head
+          ma = p.embed, r0 = S.v0, r1 = S.v1;
+          K = HID, phase = PH_HEAD, normed = true;
+          src = p.h_mlp, nsrc = HID, stag = tag - 1, nw = p.final_norm;
+          e.kind = EPI_HEAD, e.ll = nullptr, e.skip = false, e.fout = p.logits;
+        }
+        if (!paired) mb = ma;
+        const int fmt = ma.fmt;
+        const int nrows = r1 - r0;
+        // ---- loads that do not depend on this step go out before the wait
+        const int nsc = paired ? 2 * nrows : nrows;
+        const bool use_rs = fmt == 1 && nsc <= RS_MAX;
+        float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f;
+        if (use_rs) {
+          const float* sa = reinterpret_cast<const float*>(ma.scale) + r0;
+          const float* sb = reinterpret_cast<const float*>(mb.scale) + r0;
+          auto ld = [&](int v) { return v < nrows ? __ldg(sa + v) : __ldg(sb + (v - nrows)); };
+          if (tid < nsc) sc0 = ld(tid);
+          if (tid + NCT < nsc) sc1 = ld(tid + NCT);
+          if (tid + 2 * NCT < nsc) sc2 = ld(tid + 2 * NCT);
+        }
+        auto store_sc = [&] {
+          if (use_rs) {
+            if (tid < nsc) rs[tid] = sc0;
+            if (tid + NCT < nsc) rs[tid + NCT] = sc1;
+            if (tid + 2 * NCT < nsc) rs[tid + 2 * NCT] = sc2;
+          }
+        };
+        uint2 wb = make_uint2(0u, 0u);
+        if (normed) {
+          wb.x = __ldg(reinterpret_cast<const uint32_t*>(nw) + tid);
+          if (2 * (tid + NCT) < HID) wb.y = __ldg(reinterpret_cast<const uint32_t*>(nw) + tid + NCT);
+        }
+        if (step == ST_QKV && l == 0) {  // the input is the embedding row already in hs
+          stage_local(wb, fmt);
+          store_sc();
+          bar_consumers(NCT);
+        } else if (!poll_stage(src, nsrc, stag, phase == PH_QKV || phase == PH_HEAD ? PH_DOWN : phase - 1, l,
+                               normed, wb, fmt, store_sc)) {
           return;
-      }
-      signal(&p.sync->c[PH_DOWN][0], PH_DOWN, l);
-      st(PH_DOWN, 1);
-    }
-    // ---------------- final RMSNorm + LM head + argmax
-    if (!wait_ctr(&p.sync->c[PH_DOWN][0], (uint32_t)(p.n_layers * G), PH_DOWN, p.n_layers)) return;
-    st(PH_HEAD, 0);
-    load_h(p.h_mlp);
-    stage_rmsnorm(p.final_norm, p.embed.fmt);
-    float best = -INFINITY;
-    int besti = 0x7FFFFFFF;
-    {
-      float* lg = p.logits;
-      if (!rows(p.embed, HID, S.v0, S.v1, PH_HEAD, p.n_layers, [&](int r, float y) {
-            if (lg) lg[r] = y;
-            if (y > best || (y == best && r < besti)) {
-              best = y;
-              besti = r;
-            }
-          }))
-        return;
-    }
-    // CTA argmax (lowest index among equal maxima)
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-      const float ob = __shfl_xor_sync(0xffffffffu, best, o);
-      const int oi = __shfl_xor_sync(0xffffffffu, besti, o);
-      if (ob > best || (ob == best && oi < besti)) {
-        best = ob;
-        besti = oi;
+        }
+        st(phase, 0);
+        if (normed) e.inv = rms_inv();
+        gemv(paired, ma, mb, r0, r1, K, use_rs ? rs : nullptr, e);
+        bar_consumers(NCT);  // every warp is done with xs, hs and rs before they are restaged
+        st(phase, 1);
       }
     }
+    // CTA argmax (lowest index among equal maxima); lane 0 of each warp holds its warp's best
     if (lane == 0) {
       s->red[warp] = best;
       s->red[32 + warp] = __int_as_float(besti);
     }
     bar_consumers(NCT);
+    if (s->abort) return;
     if (tid == 0) {
       for (int w = 1; w < NCW; ++w) {
         const float ob = s->red[w];
@@ -720,7 +1039,7 @@ struct Consumer {
         const int32_t nxt = (int32_t)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFull));
         p.sync->tok[0] = nxt;
         if (p.next_out) *p.next_out = nxt;
-        for (int i = 0; i < 8; ++i) st_relaxed_u32(&p.sync->c[i][0], 0u);
+        st_relaxed_u32(&p.sync->c[PH_HEAD][0], 0u);
         for (int i = 0; i < NKVH; ++i) st_relaxed_u32(&p.sync->grp[i][0], 0u);
         st_relaxed_u64(&p.sync->key[0], 0ull);
       }
@@ -737,7 +1056,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode(const KParams p) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&s->full[i], 1);
-      mbar_init(&s->empty[i], NCW);
+      mbar_init(&s->empty[i], 1);  // one release per tile (see release_tiles)
     }
     s->abort = 0;
     fence_mbar_init();
@@ -769,7 +1088,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&s->full[i], 1);
-      mbar_init(&s->empty[i], NCW);
+      mbar_init(&s->empty[i], 1);
     }
     s->abort = 0;
     fence_mbar_init();
@@ -804,7 +1123,16 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
     c.warp = threadIdx.x >> 5;
     c.xr.init(nullptr);
     c.stage_global(x, cols, m.fmt);
-    c.rows(m, cols, r0, r1, PH_HEAD, 0, [&](int r, float v) { y[r] = v; });
+    typename Consumer<false>::EpiCtx e;
+    e.kind = Consumer<false>::EPI_OUT;
+    e.tag = 0;
+    e.skip = false;
+    e.inv = 1.f;
+    e.ll = nullptr;
+    e.fout = y;
+    e.dbg = nullptr;
+    c.gemv(false, m, m, r0, r1, cols, nullptr, e);
+    bar_consumers(NCT);
   }
 }
 
@@ -844,7 +1172,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_stream_read(const uint8_t* buf,
       const uint32_t slot = i % NSLOT, par = (i / NSLOT) & 1;
       uint64_t t0 = globaltimer();
       bool ok = true;
-      while (!mbar_try_wait(&s->full[slot], par))
+      while (!mbar_test_wait(&s->full[slot], par))
         if (globaltimer() - t0 > 2000000000ull) {
           ok = false;
           break;

@@ -52,7 +52,7 @@ class mk_weights(C.Structure):
 
 # every symbol include/mk.h declares
 EXPORTS = ("mk_max_context", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
-           "mk_decode_greedy", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
+           "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
            "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_gemv", "mk_stream_read", "mk_probe_cvt")
 
 _lib = None
@@ -73,6 +73,7 @@ def lib():
         L.mk_last_error.argtypes = [vp]
         L.mk_decode_step.argtypes = [vp, i32, i32, C.POINTER(i32), vp]
         L.mk_decode_greedy.argtypes = [vp, i32, i32, i32, vp]
+        L.mk_decode_next.argtypes = [vp, vp, i32, vp, vp]
         L.mk_sync.argtypes = [vp]
         L.mk_kv_cache.argtypes = [vp, C.c_int, C.POINTER(vp), C.POINTER(vp)]
         L.mk_debug_hidden.argtypes = [vp, vp]
@@ -240,6 +241,11 @@ class Model:
             out = torch.empty(n, dtype=torch.int32, device="cuda")
         self._err(lib().mk_decode_greedy(self.h, int(first_token), int(pos0), int(n), _ptr(out)), "mk_decode_greedy")
         return out
+
+    def decode_next(self, token_dev: torch.Tensor, pos: int, next_dev: torch.Tensor, logits=None):
+        """One launch; token_dev / next_dev are 1-element int32 CUDA tensors (or views)."""
+        self._err(lib().mk_decode_next(self.h, _ptr(token_dev), int(pos), _ptr(next_dev), _ptr(logits)),
+                  "mk_decode_next")
 
     def sync(self):
         self._err(lib().mk_sync(self.h), "mk_sync")

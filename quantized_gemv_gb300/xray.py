@@ -1,0 +1,117 @@
+"""X-ray analyser: turns the decode kernel's per-CTA stamps into where one token's time went.
+
+The kernel (built with MK_FLAG_XRAY) has lane 0 of warp 0 of every CTA record {%globaltimer,
+clock64, %smid, phase, kind} at the start and end of each phase and of each wait for another
+CTA's data (the stamp scheme of the X-ray milestone, monolith page, "M2: X-ray"). %globaltimer is
+one clock for the whole GPU, so records of different SMs are aligned by construction; clock64
+is per SM and is only used to check the globaltimer's granularity.
+
+The split follows the page's budget bar ("where the time goes", monolith page, "What the demo
+looks like"): weight reads (the dequant-GEMV phases), barrier wait (waits on other CTAs' data),
+attention, the LM head, and idle (a CTA's time after its own last stamp until the last CTA
+finishes).
+"""
+from __future__ import annotations
+
+import json
+
+import numpy as np
+
+PHASE_NAMES = {0: "qkv", 1: "attention", 2: "o_proj", 3: "gate_up", 4: "down", 5: "lm_head", 6: "embed"}
+GEMV_PHASES = (0, 2, 3, 4)
+KIND_BEGIN, KIND_END, KIND_WAIT_BEGIN, KIND_WAIT_END, KIND_STOP = 0, 1, 2, 3, 255
+
+
+def records(trace: np.ndarray):
+    """Yield (cta, [(t_ns, phase, kind), ...]) for every CTA that wrote records."""
+    for cta in range(trace.shape[0]):
+        rows = trace[cta]
+        out = []
+        for r in rows:
+            if r["kind"] == KIND_STOP or (r["gtime"] == 0 and r["kind"] == 0 and r["phase"] == 0):
+                break
+            out.append((int(r["gtime"]), int(r["phase"]), int(r["kind"])))
+        if out:
+            yield cta, out
+
+
+def analyze(trace: np.ndarray, bytes_by_phase: dict | None = None) -> dict:
+    """Per-token split of time (ns), averaged over CTAs, plus the critical-path length.
+
+    bytes_by_phase (optional): algorithmic bytes read per phase name over the whole token, used to
+    report the bandwidth each phase achieved over its mean active time.
+    """
+    per_cta = {}
+    t_first, t_last = None, None
+    for cta, recs in records(trace):
+        t_first = recs[0][0] if t_first is None else min(t_first, recs[0][0])
+        t_last = recs[-1][0] if t_last is None else max(t_last, recs[-1][0])
+        per_cta[cta] = recs
+    if not per_cta:
+        return {"ctas": 0}
+    token_ns = t_last - t_first
+    acc = {"weight_read": [], "barrier_wait": [], "attention": [], "lm_head": [], "idle": [], "other": []}
+    phase_active = {name: [] for name in PHASE_NAMES.values()}
+    for cta, recs in per_cta.items():
+        wait = 0
+        open_phase, open_wait = {}, None
+        active = {name: 0 for name in PHASE_NAMES.values()}
+        att_wait = 0
+        for t, ph, kind in recs:
+            if kind == KIND_BEGIN:
+                open_phase[ph] = t
+            elif kind == KIND_END and ph in open_phase:
+                active[PHASE_NAMES[ph]] += t - open_phase.pop(ph)
+            elif kind == KIND_WAIT_BEGIN:
+                open_wait = t
+            elif kind == KIND_WAIT_END and open_wait is not None:
+                wait += t - open_wait
+                if 1 in open_phase:  # a wait inside the attention phase (for q/k/v)
+                    att_wait += t - open_wait
+                open_wait = None
+        weight = sum(active[PHASE_NAMES[p]] for p in GEMV_PHASES)
+        attention = active["attention"] - att_wait
+        head = active["lm_head"]
+        idle = t_last - recs[-1][0]
+        total = recs[-1][0] - t_first
+        acc["weight_read"].append(weight)
+        acc["barrier_wait"].append(wait)
+        acc["attention"].append(attention)
+        acc["lm_head"].append(head)
+        acc["idle"].append(idle)
+        acc["other"].append(total - weight - wait - attention - head)
+        for name, v in active.items():
+            phase_active[name].append(v)
+    out = {"ctas": len(per_cta), "token_ns": int(token_ns)}
+    for k, v in acc.items():
+        out[k + "_ns"] = float(np.mean(v))
+    out["barrier_wait_share"] = out["barrier_wait_ns"] / token_ns if token_ns else 0.0
+    out["phase_mean_ns"] = {k: float(np.mean(v)) for k, v in phase_active.items() if v}
+    if bytes_by_phase:
+        out["phase_gbs"] = {k: (bytes_by_phase[k] / out["phase_mean_ns"][k]) for k in bytes_by_phase
+                            if out["phase_mean_ns"].get(k)}
+    return out
+
+
+def layer_timeline(trace: np.ndarray) -> list:
+    """Per-layer wall time (ns) on the critical path: the spread between consecutive moments at
+    which the last CTA finished its down_proj phase."""
+    ends = {}
+    for cta, recs in records(trace):
+        k = 0
+        for t, ph, kind in recs:
+            if ph == 4 and kind == KIND_END:
+                ends.setdefault(k, []).append(t)
+                k += 1
+    last = [max(ends[k]) for k in sorted(ends)]
+    return [int(b - a) for a, b in zip(last[:-1], last[1:])]
+
+
+def export_json(trace: np.ndarray, path: str, meta: dict | None = None):
+    """Compact JSON of one token's trace: one list of [t_ns, phase, kind] per CTA (t from token start)."""
+    per = dict(records(trace))
+    t0 = min(r[0][0] for r in per.values())
+    doc = {"meta": meta or {}, "phases": PHASE_NAMES,
+           "ctas": {str(c): [[t - t0, ph, k] for t, ph, k in recs] for c, recs in per.items()}}
+    with open(path, "w") as f:
+        json.dump(doc, f, separators=(",", ":"))

@@ -20,19 +20,4 @@ def golden_e2m1_grid():
 
 def oracle_pack_model(master, fmap, nthreads=None):
     """Quantise every matrix of a master-weight dict with the oracle's own quantiser."""
-    def pk(w, fmt):
-        if fmt == O.FMT_BF16:
-            return O.PackedMat(fmt, w.shape[0], w.shape[1], w)
-        if fmt == O.FMT_FP8_ROW:
-            c, s = O.quant_fp8_row(w, nthreads)
-            return O.PackedMat(fmt, w.shape[0], w.shape[1], c, s)
-        c, b, t = O.quant_nvfp4(w, nthreads)
-        return O.PackedMat(fmt, w.shape[0], w.shape[1], c, b, t)
-
-    out = {"embed": pk(master["embed"], fmap["embed"]), "final_norm": master["final_norm"], "layers": []}
-    for L in master["layers"]:
-        d = {n: pk(L[n], fmap[n]) for n in O.LINEARS}
-        for n in ("ln_in", "ln_post", "q_norm", "k_norm"):
-            d[n] = L[n]
-        out["layers"].append(d)
-    return out
+    return O.pack_model(master, fmap, nthreads)
