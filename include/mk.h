@@ -174,6 +174,28 @@ int mk_stream_read(const void* buf_dev, size_t bytes, void* stream);
 int mk_probe_cvt(uint32_t* f16_from_e4m3_dev, uint32_t* f16_from_e2m1_dev, const float* in_dev, int n,
                  uint16_t* e4m3_from_f32_dev, uint8_t* e2m1_from_f32_dev, void* stream);
 
+/* ---------------------------------------------------------------- allocation-free step */
+
+/* Largest max_ctx mk_decode_step_static accepts. */
+#define MK_STATIC_MAX_CTX 4352
+
+/* One decode step that allocates nothing, for callers that cannot allocate device memory when they
+ * decode (code running during stream capture, hosts that own every device allocation, processes
+ * that must not grow their device footprint after start-up). The pages have no counterpart: it is
+ * mk_decode_step without a model object or workspace. The caller passes the weights (as for
+ * mk_create), the bf16 KV cache as two device buffers k_dev, v_dev, each
+ * [n_layers][n_kv_heads][cfg->max_ctx][head_dim], the token and position, and receives the next
+ * token in *next_token_host (and the fp32 logits in logits_dev if not NULL).
+ * The kernel's scratch (sync words, activation exchange buffers, attention partials, layer table
+ * and RoPE table, about 2.6 MB) lives in one fixed device array that every GPU loading the library
+ * holds until the process exits; cfg->max_ctx <= MK_STATIC_MAX_CTX and n_layers <= 64.
+ * The first call on a device looks the array up on that device (the device must be current), and
+ * a call with a new rope_theta rebuilds its RoPE table. Calls share the array: two calls that run
+ * at the same time on one GPU race and give wrong results. Synchronises `stream`. Errors:
+ * MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, with text in mk_last_error(NULL). */
+int mk_decode_step_static(const mk_config* cfg, const mk_weights* w, void* k_dev, void* v_dev, int32_t token,
+                          int32_t pos, int32_t* next_token_host, float* logits_dev, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

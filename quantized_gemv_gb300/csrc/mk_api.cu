@@ -52,6 +52,8 @@ static int set_err(mk_model* m, int code, const char* fmt, ...) {
 
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+void mk::set_global_error(const char* msg) { g_create_err = msg; }
+
 struct Layout {
   size_t sync, layers, h_mlp, h_attn, qkv, att, act, attp, rope_cos, rope_sin, kc, vc, hidden, trace, total;
 };

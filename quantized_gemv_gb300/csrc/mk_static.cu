@@ -1,0 +1,187 @@
+// mk_decode_step_static: one decode step that allocates nothing.
+//
+// Some callers cannot allocate device memory when they decode: code that runs while a CUDA stream
+// is being captured (cudaMalloc is not allowed there), code inside a host framework that owns every
+// device allocation and hands out only fixed buffers, or a process that must not grow its device
+// footprint after start-up. They still own the weights and the KV cache, but they cannot provide
+// the decode kernel's scratch (sync words, the tagged activation buffers, attention partials, the
+// layer table and the RoPE table). This file keeps that scratch in one file-scope __device__ array
+// of fixed size, so the step needs no workspace and no model object.
+//
+// Limits and sharing: every GPU that loads the library holds the array until the process exits.
+// All calls on a device share it and it keeps the previous call's contents, so two calls that run
+// at the same time on one GPU (different streams, or different host threads without ordering)
+// race on it and give wrong results. The kernel resets the sync words it uses at the end of every
+// step; after a failed step they are cleared here.
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "../../include/mk.h"
+#include "mk_internal.h"
+
+using namespace mk;
+
+namespace {
+
+constexpr int STATIC_MAX_LAYERS = 64;
+constexpr int STATIC_MAX_CTX = MK_STATIC_MAX_CTX;
+
+struct __align__(256) StaticScratch {
+  SyncBlock sync;
+  DLayer layers[STATIC_MAX_LAYERS];
+  llword h_mlp[HID];
+  llword h_attn[HID];
+  llword qkv[QKV_ROWS];
+  llword att[QROWS];
+  llword act[FFN];
+  float attp[NKVH * MAXC * 2 * PART_STRIDE];
+  float rope_cos[STATIC_MAX_CTX * (HD / 2)];
+  float rope_sin[STATIC_MAX_CTX * (HD / 2)];
+};
+
+// The scratch itself (zero-initialised when the module loads).
+__device__ __align__(256) StaticScratch g_static_scratch;
+
+// Per-device state of the host side.
+struct DevState {
+  bool ready = false;
+  StaticScratch* ptr = nullptr;  // device address of g_static_scratch on this device
+  float rope_theta = 0.f;        // theta the RoPE table was built for (0 = not built)
+  uint32_t steps = 0;
+  int grid = 0;
+};
+constexpr int MAX_DEVICES = 64;
+DevState g_dev[MAX_DEVICES];
+std::mutex g_mu;
+int fail(int code, const char* msg) {
+  set_global_error(msg);
+  return code;
+}
+
+}  // namespace
+
+extern "C" {
+
+int mk_decode_step_static(const mk_config* c, const mk_weights* w, void* kv_k_dev, void* kv_v_dev, int32_t token,
+                          int32_t pos, int32_t* next_token_host, float* logits_dev, void* stream) {
+  if (!c || !w || !w->layers || !kv_k_dev || !kv_v_dev || !next_token_host)
+    return fail(MK_EINVAL, "NULL argument");
+  if (c->hidden != HID || c->n_q_heads != NQH || c->n_kv_heads != NKVH || c->head_dim != HD || c->ffn != FFN)
+    return fail(MK_EINVAL, "only the Qwen3-0.6B shape family (1024/16/8/128/3072) is supported");
+  if (c->n_layers < 1 || c->n_layers > STATIC_MAX_LAYERS || c->vocab < 1 || c->vocab >= (1 << 24))
+    return fail(MK_EINVAL, "bad n_layers or vocab");
+  if (c->max_ctx < 1 || c->max_ctx > STATIC_MAX_CTX)
+    return fail(MK_EINVAL, "max_ctx must be at most MK_STATIC_MAX_CTX for the static entry point");
+  if (token < 0 || token >= c->vocab || pos < 0 || pos >= c->max_ctx) return fail(MK_EINVAL, "token or pos out of range");
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return fail(MK_EINVAL, "bad eps/theta");
+  if (((uintptr_t)kv_k_dev & 15u) || ((uintptr_t)kv_v_dev & 15u)) return fail(MK_EINVAL, "KV cache not 16-byte aligned");
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return fail(MK_ECUDA, "no current device");
+  cudaStream_t st = (cudaStream_t)stream;
+
+  std::lock_guard<std::mutex> lock(g_mu);
+  DevState& D = g_dev[dev];
+  if (!D.ready) {  // set-up, once per device, with that device current
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return fail(MK_ECUDA, "cannot query the device");
+    int bps = 0;
+    if (sms < 64 || decode_occupancy(&bps) || bps < 1) return fail(MK_ENORESIDENT, "persistent grid does not fit");
+    D.ptr = static_cast<StaticScratch*>(p);
+    D.grid = sms;
+    D.ready = true;
+  }
+  const int max_units = (D.grid / NKVH) > MAXC ? MAXC : (D.grid / NKVH);
+  if (c->max_ctx > max_units * UNIT_POS) return fail(MK_EINVAL, "max_ctx exceeds this device's attention window");
+  StaticScratch* S = D.ptr;
+  cudaError_t e = cudaSuccess;
+  if (D.rope_theta != c->rope_theta) {  // (re)build the RoPE table for this theta
+    if (launch_rope_table(S->rope_cos, S->rope_sin, STATIC_MAX_CTX, c->rope_theta, st)) e = cudaGetLastError();
+    if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
+    D.rope_theta = c->rope_theta;
+  }
+  // the layer table of this call (pageable source: the copy completes before this call returns it)
+  DLayer dl[STATIC_MAX_LAYERS];
+  for (int l = 0; l < c->n_layers; ++l) {
+    const mk_layer& ly = w->layers[l];
+    const mk_mat* mats[7] = {&ly.q, &ly.k, &ly.v, &ly.o, &ly.gate, &ly.up, &ly.down};
+    for (int i = 0; i < 7; ++i) {
+      const mk_mat& m = *mats[i];
+      if (m.fmt < MK_BF16 || m.fmt > MK_NVFP4 || !m.data || ((uintptr_t)m.data & 15u) ||
+          (m.fmt != MK_BF16 && (!m.scale || ((uintptr_t)m.scale & 15u))))
+        return fail(MK_EINVAL, "bad weight matrix");
+      dl[l].m[i].data = (const uint8_t*)m.data;
+      dl[l].m[i].scale = (const uint8_t*)m.scale;
+      dl[l].m[i].tscale = m.tensor_scale;
+      dl[l].m[i].fmt = m.fmt;
+    }
+    if (ly.q.fmt != ly.k.fmt || ly.q.fmt != ly.v.fmt || ly.gate.fmt != ly.up.fmt)
+      return fail(MK_EINVAL, "q/k/v and gate/up must share formats");
+    if (!ly.ln_in || !ly.ln_post || !ly.q_norm || !ly.k_norm) return fail(MK_EINVAL, "norm weight NULL");
+    dl[l].ln_in = (const uint16_t*)ly.ln_in;
+    dl[l].ln_post = (const uint16_t*)ly.ln_post;
+    dl[l].q_norm = (const uint16_t*)ly.q_norm;
+    dl[l].k_norm = (const uint16_t*)ly.k_norm;
+  }
+  if (w->embed.fmt != MK_BF16 && w->embed.fmt != MK_FP8_ROW) return fail(MK_EINVAL, "embedding must be bf16 or FP8");
+  if (!w->embed.data || (w->embed.fmt == MK_FP8_ROW && !w->embed.scale) || !w->final_norm)
+    return fail(MK_EINVAL, "embedding or final norm NULL");
+  e = cudaMemcpyAsync(S->layers, dl, sizeof(DLayer) * c->n_layers, cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
+
+  KParams p = {};
+  p.layers = S->layers;
+  p.n_layers = c->n_layers;
+  p.embed.data = (const uint8_t*)w->embed.data;
+  p.embed.scale = (const uint8_t*)w->embed.scale;
+  p.embed.tscale = w->embed.tensor_scale;
+  p.embed.fmt = w->embed.fmt;
+  p.final_norm = (const uint16_t*)w->final_norm;
+  p.vocab = c->vocab;
+  p.max_ctx = c->max_ctx;
+  p.eps = c->rms_eps;
+  p.kc = (uint16_t*)kv_k_dev;
+  p.vc = (uint16_t*)kv_v_dev;
+  p.rope_cos = S->rope_cos;
+  p.rope_sin = S->rope_sin;
+  p.h_mlp = S->h_mlp;
+  p.h_attn = S->h_attn;
+  p.qkv = S->qkv;
+  p.att = S->att;
+  p.act = S->act;
+  p.attp = S->attp;
+  p.sync = &S->sync;
+  p.hidden_dbg = nullptr;
+  p.logits = logits_dev;
+  p.trace = nullptr;
+  p.token = token;
+  p.token_ptr = nullptr;
+  p.pos = pos;
+  p.next_out = nullptr;
+  p.units = (pos + 1 <= UNIT_POS) ? 1 : max_units;
+  D.steps = (D.steps + 1) & 0x03FFFFFFu;
+  if (D.steps == 0) D.steps = 1;
+  p.tagbase = D.steps * 64u;
+  p.timeout_ns = 500000000ull;
+  p.fault_cta = -1;
+  p.fault_phase = -1;
+  if (launch_decode(p, D.grid, false, st)) return fail(MK_ECUDA, cudaGetErrorString(cudaGetLastError()));
+  // the step's status and token (SyncBlock::status then ::tok, 64 words)
+  uint32_t hs[64];
+  e = cudaMemcpyAsync(hs, S->sync.status, sizeof hs, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
+  if (hs[0] != 0) {  // a failed step leaves sync words behind: clear them for the next call
+    cudaMemsetAsync(&S->sync, 0, sizeof(SyncBlock), st);
+    cudaStreamSynchronize(st);
+    return fail(hs[0] == 4 ? MK_EINVAL : MK_ETIMEOUT, "device step failed");
+  }
+  *next_token_host = (int32_t)hs[32];
+  return MK_OK;
+}
+
+}  // extern "C"

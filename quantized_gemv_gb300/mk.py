@@ -53,7 +53,8 @@ class mk_weights(C.Structure):
 # every symbol include/mk.h declares
 EXPORTS = ("mk_max_context", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
            "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
-           "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_gemv", "mk_stream_read", "mk_probe_cvt")
+           "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
+           "mk_decode_step_static")
 
 _lib = None
 
@@ -84,6 +85,8 @@ def lib():
         L.mk_gemv.argtypes = [C.POINTER(mk_mat), C.c_int, C.c_int, vp, vp, vp]
         L.mk_stream_read.argtypes = [vp, sz, vp]
         L.mk_probe_cvt.argtypes = [vp, vp, vp, C.c_int, vp, vp, vp]
+        L.mk_decode_step_static.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), vp, vp, i32, i32,
+                                            C.POINTER(i32), vp, vp]
         _lib = L
     return _lib
 
@@ -278,6 +281,29 @@ class Model:
 
     def debug_fault(self, cta: int, phase: int, timeout_ms: int = 0):
         self._err(lib().mk_debug_fault(self.h, cta, phase, timeout_ms), "mk_debug_fault")
+
+
+MK_STATIC_MAX_CTX = 4352
+
+
+def decode_step_static(cfg: ModelConfig, packed, k_cache: torch.Tensor, v_cache: torch.Tensor, token: int,
+                       pos: int, logits: torch.Tensor | None = None, stream=None) -> int:
+    """mk_decode_step_static: one step with no model object and no workspace (the library keeps its
+    scratch in a fixed device array). k_cache / v_cache: bf16 CUDA tensors of
+    n_layers * n_kv_heads * max_ctx * head_dim elements (state the caller keeps between steps)."""
+    ccfg = mk_config(cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn, cfg.vocab,
+                     cfg.max_ctx, cfg.rope_theta, cfg.rms_eps)
+    layers = (mk_layer * cfg.n_layers)()
+    for i, Lp in enumerate(packed["layers"]):
+        layers[i] = mk_layer(*(Lp[n].c() for n in LINEARS), Lp["ln_in"].data_ptr(), Lp["ln_post"].data_ptr(),
+                             Lp["q_norm"].data_ptr(), Lp["k_norm"].data_ptr())
+    w = mk_weights(C.cast(layers, C.c_void_p), packed["embed"].c(), packed["final_norm"].data_ptr())
+    nxt = C.c_int32()
+    rc = lib().mk_decode_step_static(C.byref(ccfg), C.byref(w), _ptr(k_cache), _ptr(v_cache), int(token), int(pos),
+                                     C.byref(nxt), _ptr(logits), _stream(stream))
+    if rc != MK_OK:
+        raise MkError(rc, lib().mk_last_error(None).decode())
+    return int(nxt.value)
 
 
 def upload_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
