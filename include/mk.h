@@ -85,7 +85,7 @@ typedef struct mk_model mk_model; /* opaque; library-owned host object */
 /* ---------------------------------------------------------------- model lifetime */
 
 /* Largest max_ctx this build accepts on the current device (attention splits the context into
- * at most one unit per SM, each holding up to 320 positions in shared memory). */
+ * at most one unit per SM, each holding up to 288 positions in shared memory). */
 int mk_max_context(void);
 
 /* Bytes of device workspace a model needs: bf16 KV cache [n_layers][n_kv][max_ctx][head_dim] for
