@@ -62,7 +62,7 @@ static int device_grid(int* grid) {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return -1;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
-  *grid = sms;
+  *grid = decode_grid_for(sms);
   return 0;
 }
 

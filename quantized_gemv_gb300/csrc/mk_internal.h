@@ -107,6 +107,12 @@ struct KParams {
   int fault_phase;
 };
 
+// CTAs of the persistent decode grid on a device with `sms` SMs (one CTA per SM): 128 where the
+// device has them, so that every CTA's share of each exchanged vector (8 of the 1024 hidden rows,
+// 24 of the 3072 FFN units, 32 q/k/v rows) is a whole number of 32-byte sectors; otherwise the
+// largest multiple of 8 (one group per KV head).
+inline int decode_grid_for(int sms) { return sms >= 128 ? 128 : (sms / NKVH) * NKVH; }
+
 // Launchers (mk_kernel.cu / mk_aux.cu)
 int launch_decode(const KParams& p, int grid, bool xray, void* stream);
 int decode_smem_bytes();

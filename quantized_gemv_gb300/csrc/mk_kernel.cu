@@ -109,6 +109,24 @@ __device__ __forceinline__ int tile_rows(int fmt, int K) {
   int r = SLOT / (code_bytes(fmt, K) + scale_bytes(fmt, K));
   return r > 32 ? 32 : r;
 }
+// The same geometry as compile-time constants for the consumer's hot path: rows per tile, and the
+// multiplier m with i / rows == umulhi(i, m) for the row indices of one phase (i < 2^24).
+template <int FMT, int K>
+struct Geom {
+  static constexpr int CB = FMT == 0 ? 2 * K : (FMT == 1 ? K : K / 2);
+  static constexpr int SB = FMT == 2 ? K / 16 : 0;
+  static constexpr int RPT = SLOT / (CB + SB) > 32 ? 32 : SLOT / (CB + SB);
+  static constexpr uint32_t MAG = 0xFFFFFFFFu / (uint32_t)RPT + 1u;
+};
+template <int FMT>
+__device__ __forceinline__ void geom_of(int K, int& rpt, uint32_t& mag) {
+  switch (K) {
+    case 1024: rpt = Geom<FMT, 1024>::RPT, mag = Geom<FMT, 1024>::MAG; break;
+    case 2048: rpt = Geom<FMT, 2048>::RPT, mag = Geom<FMT, 2048>::MAG; break;
+    case 3072: rpt = Geom<FMT, 3072>::RPT, mag = Geom<FMT, 3072>::MAG; break;
+    default: rpt = Geom<FMT, 4096>::RPT, mag = Geom<FMT, 4096>::MAG; break;
+  }
+}
 // Position of input element k in the staged vector, laid out so that lane l of a warp reads the
 // activations of its 16-byte weight slice as conflict-free float4 loads.
 __device__ __forceinline__ int xs_index(int k, int epl) {
@@ -167,6 +185,9 @@ struct Producer {
       if (!mbar_test_wait(&s->empty[slot], par)) {
         uint64_t t0 = globaltimer();
         while (!mbar_test_wait(&s->empty[slot], par)) {
+#ifndef MKX_NOSLEEP
+          __nanosleep(256);  // the ring is full: leave the issue slots to the consumer warps
+#endif
           if (s->abort) return false;
           if (globaltimer() - t0 > deadline_ns) return false;
         }
@@ -192,6 +213,18 @@ struct Producer {
     for (int r = r0; r < r1 && ok; r += rpt) {
       int nr = min(rpt, r1 - r);
       issue(m.data + (size_t)r * cb, (uint32_t)(nr * cb), sb ? m.scale + (size_t)r * sb : nullptr,
+            (uint32_t)(nr * sb));
+    }
+  }
+  // Rows [r0, r1) of two matrices of one format (gate and up), their tiles interleaved: a's tile t,
+  // then b's tile t, so a consumer needs two slots at a time for one FFN unit.
+  __device__ void rows_paired(const DMat& a, const DMat& b, int K, int r0, int r1) {
+    const int cb = code_bytes(a.fmt, K), sb = scale_bytes(a.fmt, K), rpt = tile_rows(a.fmt, K);
+    for (int r = r0; r < r1 && ok; r += rpt) {
+      int nr = min(rpt, r1 - r);
+      issue(a.data + (size_t)r * cb, (uint32_t)(nr * cb), sb ? a.scale + (size_t)r * sb : nullptr,
+            (uint32_t)(nr * sb));
+      issue(b.data + (size_t)r * cb, (uint32_t)(nr * cb), sb ? b.scale + (size_t)r * sb : nullptr,
             (uint32_t)(nr * sb));
     }
   }
@@ -243,8 +276,7 @@ __device__ void run_producer(const KParams& P, Smem* s, uint8_t* ring) {
     pr.rows(L.m[M_Q + S.qm], HID, S.qr0, S.qr1);
     if (S.unit) pr.kv(l, S.ug, S.t0, S.ncached);
     pr.rows(L.m[M_O], QROWS, S.o0, S.o1);
-    pr.rows(L.m[M_GATE], HID, S.j0, S.j1);
-    pr.rows(L.m[M_UP], HID, S.j0, S.j1);
+    pr.rows_paired(L.m[M_GATE], L.m[M_UP], HID, S.j0, S.j1);
     pr.rows(L.m[M_DOWN], FFN, S.d0, S.d1);
   }
   if (pr.ok) pr.rows(P.embed, HID, S.v0, S.v1);
@@ -268,6 +300,7 @@ struct Consumer {
   const KParams* P;
   uint32_t n;  // tiles consumed
   int tid, lane, warp;
+  float eps;   // RMSNorm epsilon
   Xray<XR> xr;
 
   __device__ void fail(uint32_t code, uint32_t detail) {
@@ -292,7 +325,7 @@ struct Consumer {
   __device__ void wait_full(uint32_t slot, uint32_t par, int phase, int layer) {
     if (mbar_test_wait(&s->full[slot], par)) return;
     uint64_t t0 = globaltimer();
-    while (!mbar_test_wait(&s->full[slot], par)) {
+    while (!mbar_try_wait(&s->full[slot], par)) {  // suspends the warp for a while in hardware
       if (s->abort) return;
       if (globaltimer() - t0 > P->timeout_ns) {
         fail(3u, (uint32_t)(phase | (layer << 8) | (blockIdx.x << 16)) | 0x80000000u);
@@ -390,11 +423,10 @@ struct Consumer {
   }
   // 1 / sqrt(mean(h^2) + eps) from the per-warp sums in red[] (after a CTA barrier).
   __device__ __forceinline__ float rms_inv() const {
-    float tot = lane < NCW ? s->red[lane] : 0.f;
+    float tot = 0.f;
 #pragma unroll
-    for (int o = 8; o; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
-    tot = __shfl_sync(0xffffffffu, tot, 0);
-    return 1.0f / sqrtf(tot / (float)HID + P->eps);
+    for (int w = 0; w < NCW; ++w) tot += s->red[w];  // same order in every thread
+    return rsqrtf(tot * (1.0f / (float)HID) + eps);
   }
   // Load n floats (plain fp32, e.g. the standalone GEMV input) into the staged layout.
   __device__ void stage_global(const float* src, int n, int fmt) {
@@ -403,17 +435,24 @@ struct Consumer {
     bar_consumers(NCT);
   }
 
-  // Ring protocol at phase granularity: lane i of warp 0 waits for (or releases) tile first + i,
-  // so a phase costs two rounds of mbarrier operations however many rows and warps it has.
-  // wait_tiles must be followed by a CTA barrier before the tiles are read; release_tiles must be
-  // preceded by one after the last read.
-  __device__ __forceinline__ void wait_tiles(int first, int count, int phase, int layer) {
-    if (warp == 0 && lane < count)
-      wait_full((n + first + lane) % NSLOT, ((n + first + lane) / NSLOT) & 1, phase, layer);
+  // Ring protocol. A slot is free again once every consumer warp has arrived on its empty barrier
+  // (count NCW). In the GEMV engine each warp waits for (lane i: tile first + i) and releases the
+  // tiles of a batch by itself, so no CTA barrier sits inside a phase. Attention uses the CTA-wide
+  // form: warp 0 waits (a CTA barrier follows before the tiles are read) and, after a CTA barrier
+  // behind the last read, releases on behalf of all warps.
+  __device__ __forceinline__ void warp_wait_tiles(int first, int count, int phase, int layer) {
+    if (lane < count) wait_full((n + first + lane) % NSLOT, ((n + first + lane) / NSLOT) & 1, phase, layer);
     __syncwarp();
   }
+  __device__ __forceinline__ void warp_release_tiles(int first, int count) {
+    __syncwarp();
+    if (lane < count) mbar_arrive(&s->empty[(n + first + lane) % NSLOT]);
+  }
+  __device__ __forceinline__ void wait_tiles(int first, int count, int phase, int layer) {
+    if (warp == 0) warp_wait_tiles(first, count, phase, layer);
+  }
   __device__ __forceinline__ void release_tiles(int first, int count) {
-    if (warp == 0 && lane < count) mbar_arrive(&s->empty[(n + first + lane) % NSLOT]);
+    if (warp == 0 && lane < count) mbar_arrive_cnt(&s->empty[(n + first + lane) % NSLOT], NCW);
   }
 
   // Lane partial dot products of NR rows against the staged activations.
@@ -490,20 +529,34 @@ struct Consumer {
   }
 
   // ---------------------------------------------------------------- dequant-GEMV engine
-  // One phase = rows [r0, r1) of matrix a (and, PAIRED, the same rows of matrix b: gate with up),
-  // streamed by the producer as tiles of `rpt` rows (a's tiles, then b's). Warp w computes rows
-  // w + k NCW, four at a time (four independent dot products; PAIRED: units u and u + NCW, each
-  // with its gate and up row). Every warp waits for and releases every tile of the phase exactly
-  // once, in order per matrix. srow: FP8 row scales staged in shared memory (a's rows, then b's).
+  // One phase = rows [r0, r1) of matrix a (PAIRED: FFN units, each a row of a = gate and the same
+  // row of b = up, their tiles interleaved a0 b0 a1 b1 ...), streamed as tiles of `rpt` rows.
+  // Warps take groups of UPG consecutive units in turn (warp w: units [UPG (w + k NCW), +UPG)), so
+  // the NR rows of a pass are independent dot products whose results go to consecutive outputs.
+  // Every warp walks the phase's tiles in order and releases each one as soon as it has no rows
+  // left in it (waiting first on tiles it does not read, so every release follows the fill), so
+  // it never holds more than its current group's tiles: no CTA barrier, no deadlock on the ring.
+  __device__ __forceinline__ void flush_tiles(int& released, int upto) {
+    while (released < upto) {
+      const int c = min(4, upto - released);
+      warp_wait_tiles(released, c, PH_WAIT, -1);
+      warp_release_tiles(released, c);
+      released += c;
+    }
+  }
   template <int FMT, bool REGX, bool PAIRED, int NR>
   __device__ void gemv_t(const DMat& ma, const DMat& mb, int r0, int r1, int K, const float* srow, const EpiCtx& e) {
     constexpr int EPL = FMT == 0 ? 8 : (FMT == 1 ? 16 : 32);
+    constexpr int UPG = PAIRED ? NR / 2 : NR;  // units per group
+    constexpr int TPU = PAIRED ? 2 : 1;        // tiles per block of rpt units
     const int nchunk = K / (32 * EPL);
-    const int cb = code_bytes(FMT, K), sbytes = scale_bytes(FMT, K), rpt = tile_rows(FMT, K);
-    const uint32_t rmag = 0xFFFFFFFFu / (uint32_t)rpt + 1u;  // i / rpt == umulhi(i, rmag) for i < 2^27
+    const int cb = code_bytes(FMT, K), sbytes = scale_bytes(FMT, K);
+    int rpt;
+    uint32_t rmag;
+    geom_of<FMT>(K, rpt, rmag);
     const int nrows = r1 - r0;
-    const int T = (nrows + rpt - 1) / rpt;  // tiles of one matrix
-    const int ntiles = PAIRED ? 2 * T : T;
+    const int T = (int)__umulhi((uint32_t)(nrows + rpt - 1), rmag);  // tile blocks
+    const int ntiles = TPU * T;
     float4 xr[8];
     if constexpr (REGX) {
       const float4* xs4 = reinterpret_cast<const float4*>(s->xs) + lane;
@@ -512,34 +565,27 @@ struct Consumer {
     }
     const float* sca = reinterpret_cast<const float*>(ma.scale) + r0;
     const float* scb = reinterpret_cast<const float*>(mb.scale) + r0;
-    constexpr int UPP = PAIRED ? 2 : NR;  // units (rows of a) per pass
-    // batches of tiles: PAIRED phases take all 2T tiles at once (they fit the ring); others take
-    // up to 5, so a long phase (the LM head) keeps the producer streaming while it computes
-    const int tpb = PAIRED ? T : (T < 5 ? T : 5);
-    for (int bt = 0; bt < T; bt += tpb) {
-      const int nb = min(tpb, T - bt);
-      wait_tiles(bt, nb, PH_WAIT, -1);
-      if (PAIRED) wait_tiles(T + bt, nb, PH_WAIT, -1);
-      bar_consumers(NCT);
-      const int row_end = min((bt + nb) * rpt, nrows);
-      for (int base = bt * rpt + warp; base < row_end; base += UPP * NCW) {
-        int ridx[NR];
-        bool valid[NR];
+    int released = 0;
+    for (int b0 = 0; b0 < nrows; b0 += UPG * NCW) {
+      const int g0 = b0 + UPG * warp;
+      if (g0 < nrows) {
+        const int glast = min(g0 + UPG, nrows) - 1;
+        const int ta = TPU * (int)__umulhi((uint32_t)g0, rmag);
+        const int tb = TPU * (int)__umulhi((uint32_t)glast, rmag) + TPU - 1;
+        flush_tiles(released, ta);
+        warp_wait_tiles(ta, tb - ta + 1, PH_WAIT, -1);
         const uint8_t* code[NR];
         const uint8_t* bsc[NR];
         float sc[NR];
 #pragma unroll
         for (int k = 0; k < NR; ++k) {
-          const int u = base + (PAIRED ? (k >> 1) : k) * NCW;  // row of a (or unit)
+          const int u = g0 + (PAIRED ? (k >> 1) : k);
           const bool isb = PAIRED && (k & 1);
-          valid[k] = u < row_end;
-          const int uu = valid[k] ? u : base;
+          const int uu = u < nrows ? u : g0;
           const int tl = (int)__umulhi((uint32_t)uu, rmag);
           const int rit = uu - tl * rpt;
           const int nr = tl == T - 1 ? nrows - tl * rpt : rpt;
-          const int tt = isb ? T + tl : tl;
-          ridx[k] = uu;
-          const uint8_t* tile = ring + (size_t)((n + tt) % NSLOT) * SLOT;
+          const uint8_t* tile = ring + (size_t)((n + TPU * tl + (isb ? 1 : 0)) % NSLOT) * SLOT;
           code[k] = tile + (size_t)rit * cb;
           bsc[k] = tile + (size_t)nr * cb + (size_t)rit * sbytes;
           if constexpr (FMT == 1) {
@@ -556,25 +602,26 @@ struct Consumer {
 #pragma unroll
           for (int k = 0; k < NR; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k], o);
         }
-        if (lane == 0) {
-          if constexpr (PAIRED) {
+        // every lane holds every sum: lane j writes unit g0 + j (selects, no dynamic register index)
+        if constexpr (PAIRED) {
+          float g = part[0] * sc[0], up = part[1] * sc[1];
 #pragma unroll
-            for (int k = 0; k < NR; k += 2) {
-              if (valid[k]) {
-                const float g = part[k] * sc[k] * e.inv, up = part[k + 1] * sc[k + 1] * e.inv;
-                if (!e.skip) ll_store(e.ll + ridx[k], e.tag, g / (1.0f + expf(-g)) * up);
-              }
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < NR; ++k)
-              if (valid[k]) epi_row(e, r0 + ridx[k], part[k] * sc[k]);
+          for (int k = 2; k < NR; k += 2)
+            if (lane == k / 2) g = part[k] * sc[k], up = part[k + 1] * sc[k + 1];
+          if (lane < UPG && g0 + lane < nrows) {
+            g *= e.inv, up *= e.inv;
+            if (!e.skip) ll_store(e.ll + g0 + lane, e.tag, g / (1.0f + expf(-g)) * up);
           }
+        } else {
+          float y = part[0] * sc[0];
+#pragma unroll
+          for (int k = 1; k < NR; ++k)
+            if (lane == k) y = part[k] * sc[k];
+          if (lane < UPG && g0 + lane < nrows) epi_row(e, r0 + g0 + lane, y);
         }
       }
-      bar_consumers(NCT);  // every read of the batch is done
-      release_tiles(bt, nb);
-      if (PAIRED) release_tiles(T + bt, nb);
+      const int gnext = g0 + UPG * NCW;  // this warp's next group
+      flush_tiles(released, gnext < nrows ? TPU * (int)__umulhi((uint32_t)gnext, rmag) : ntiles);
     }
     n += ntiles;
   }
@@ -585,9 +632,9 @@ struct Consumer {
     const int fmt = ma.fmt;
     const bool one = r1 - r0 <= NCW;  // at most one row per warp: one row per pass
     if (paired) {
-      if (fmt == 0) gemv_t<0, true, true, 4>(ma, mb, r0, r1, K, srow, e);
-      else if (fmt == 1) gemv_t<1, true, true, 4>(ma, mb, r0, r1, K, srow, e);
-      else gemv_t<2, true, true, 4>(ma, mb, r0, r1, K, srow, e);
+      if (fmt == 0) gemv_t<0, true, true, 6>(ma, mb, r0, r1, K, srow, e);
+      else if (fmt == 1) gemv_t<1, true, true, 6>(ma, mb, r0, r1, K, srow, e);
+      else gemv_t<2, true, true, 6>(ma, mb, r0, r1, K, srow, e);
     } else if (K == 1024) {
       if (fmt == 0) gemv_t<0, true, false, 4>(ma, mb, r0, r1, K, srow, e);
       else if (fmt == 1) gemv_t<1, true, false, 4>(ma, mb, r0, r1, K, srow, e);
@@ -1012,7 +1059,17 @@ struct Consumer {
         st(phase, 1);
       }
     }
-    // CTA argmax (lowest index among equal maxima); lane 0 of each warp holds its warp's best
+    // CTA argmax (lowest index among equal maxima): lanes 0..3 of each warp tracked the rows they
+    // wrote; fold them into lane 0, then over the warps
+#pragma unroll
+    for (int o = 2; o; o >>= 1) {
+      const float ob = __shfl_down_sync(0xffffffffu, best, o);
+      const int oi = __shfl_down_sync(0xffffffffu, besti, o);
+      if (ob > best || (ob == best && oi < besti)) {
+        best = ob;
+        besti = oi;
+      }
+    }
     if (lane == 0) {
       s->red[warp] = best;
       s->red[32 + warp] = __int_as_float(besti);
@@ -1056,7 +1113,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode(const KParams p) {
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&s->full[i], 1);
-      mbar_init(&s->empty[i], 1);  // one release per tile (see release_tiles)
+      mbar_init(&s->empty[i], NCW);  // every consumer warp releases every tile
     }
     s->abort = 0;
     fence_mbar_init();
@@ -1073,6 +1130,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode(const KParams p) {
     c.tid = threadIdx.x;
     c.lane = threadIdx.x & 31;
     c.warp = threadIdx.x >> 5;
+    c.eps = p.eps;
     c.xr.init(p.trace);
     c.run(p);
     if (c.tid == 0) c.xr.finish();
@@ -1088,7 +1146,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&s->full[i], 1);
-      mbar_init(&s->empty[i], 1);
+      mbar_init(&s->empty[i], NCW);
     }
     s->abort = 0;
     fence_mbar_init();
@@ -1121,6 +1179,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
     c.tid = threadIdx.x;
     c.lane = threadIdx.x & 31;
     c.warp = threadIdx.x >> 5;
+    c.eps = 0.f;
     c.xr.init(nullptr);
     c.stage_global(x, cols, m.fmt);
     typename Consumer<false>::EpiCtx e;

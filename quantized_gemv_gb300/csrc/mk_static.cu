@@ -92,7 +92,7 @@ int mk_decode_step_static(const mk_config* c, const mk_weights* w, void* kv_k_de
     int bps = 0;
     if (sms < 64 || decode_occupancy(&bps) || bps < 1) return fail(MK_ENORESIDENT, "persistent grid does not fit");
     D.ptr = static_cast<StaticScratch*>(p);
-    D.grid = sms;
+    D.grid = decode_grid_for(sms);
     D.ready = true;
   }
   const int max_units = (D.grid / NKVH) > MAXC ? MAXC : (D.grid / NKVH);

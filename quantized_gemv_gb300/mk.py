@@ -277,7 +277,8 @@ class Model:
         buf = np.zeros(cap, dtype=np.uint8)
         written = C.c_size_t()
         self._err(lib().mk_trace_dump(self.h, buf.ctypes.data_as(C.c_void_p), cap, C.byref(written)), "mk_trace_dump")
-        return buf[: written.value].view(TRACE_DTYPE).reshape(grid, 512)
+        recs = buf[: written.value].view(TRACE_DTYPE)
+        return recs.reshape(len(recs) // 512, 512)  # one row of records per CTA of the grid
 
     def debug_fault(self, cta: int, phase: int, timeout_ms: int = 0):
         self._err(lib().mk_debug_fault(self.h, cta, phase, timeout_ms), "mk_debug_fault")
