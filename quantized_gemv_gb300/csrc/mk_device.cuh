@@ -146,8 +146,21 @@ __device__ __forceinline__ float2 e2m1x2_to_f2(uint32_t byte) {
   return __half22float2(*reinterpret_cast<__half2*>(&h));
 }
 
+// (a0, a1) += (w0 * x0, w1 * x1) as one packed instruction; each lane is exactly fmaf.
+__device__ __forceinline__ void ffma2(float& a0, float& a1, float w0, float w1, float x0, float x1) {
+  asm("{ .reg .b64 A, W, X;\n\t"
+      "mov.b64 A, {%0, %1};\n\t"
+      "mov.b64 W, {%2, %3};\n\t"
+      "mov.b64 X, {%4, %5};\n\t"
+      "fma.rn.f32x2 A, W, X, A;\n\t"
+      "mov.b64 {%0, %1}, A; }"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
+}
+
 // 16 bytes of weights times the matching activations, accumulated into acc[0..1] (two independent
-// chains keep the FMA dependency short). bf16: 8 weights, x: 2 float4. FP8: 16 weights, x: 4 float4.
+// chains keep the FMA dependency short: even elements into acc[0], odd into acc[1]).
+// bf16: 8 weights, x: 2 float4. FP8: 16 weights, x: 4 float4.
 __device__ __forceinline__ void dot_bf16_16B(uint4 w, const float4* x, float* acc) {
   const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
@@ -155,8 +168,7 @@ __device__ __forceinline__ void dot_bf16_16B(uint4 w, const float4* x, float* ac
     float lo = __uint_as_float(ws[i] << 16), hi = __uint_as_float(ws[i] & 0xFFFF0000u);
     const float4 xv = x[i / 2];
     float xa = (i & 1) ? xv.z : xv.x, xb = (i & 1) ? xv.w : xv.y;
-    acc[0] = fmaf(lo, xa, acc[0]);
-    acc[1] = fmaf(hi, xb, acc[1]);
+    ffma2(acc[0], acc[1], lo, hi, xa, xb);
   }
 }
 __device__ __forceinline__ void dot_fp8_16B(uint4 w, const float4* x, float* acc) {
@@ -165,10 +177,8 @@ __device__ __forceinline__ void dot_fp8_16B(uint4 w, const float4* x, float* acc
   for (int i = 0; i < 4; ++i) {
     float2 a = e4m3x2_to_f2(ws[i] & 0xFFFFu), b = e4m3x2_to_f2(ws[i] >> 16);
     const float4 xv = x[i];
-    acc[0] = fmaf(a.x, xv.x, acc[0]);
-    acc[1] = fmaf(a.y, xv.y, acc[1]);
-    acc[0] = fmaf(b.x, xv.z, acc[0]);
-    acc[1] = fmaf(b.y, xv.w, acc[1]);
+    ffma2(acc[0], acc[1], a.x, a.y, xv.x, xv.y);
+    ffma2(acc[0], acc[1], b.x, b.y, xv.z, xv.w);
   }
 }
 // NVFP4: 16 bytes = 32 weights = two 16-element scale blocks; x: 8 float4; s0/s1: block scales.
@@ -183,8 +193,7 @@ __device__ __forceinline__ void dot_nvfp4_16B(uint4 w, const float4* x, float s0
       const int e = i * 8 + b * 2;  // element index within the lane's 32
       const float4 xv = x[e / 4];
       float xa = (e % 4 == 0) ? xv.x : xv.z, xb = (e % 4 == 0) ? xv.y : xv.w;
-      blk[i / 2][0] = fmaf(v.x, xa, blk[i / 2][0]);
-      blk[i / 2][1] = fmaf(v.y, xb, blk[i / 2][1]);
+      ffma2(blk[i / 2][0], blk[i / 2][1], v.x, v.y, xa, xb);
     }
   }
   acc[0] = fmaf(blk[0][0] + blk[0][1], s0, acc[0]);

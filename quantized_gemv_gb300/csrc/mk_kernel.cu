@@ -91,6 +91,9 @@ struct __align__(16) Smem {
   float vn[HD];
   float sc[2][UNIT_POS];
   float stat[4];
+  float wst[NCW][4];                 // attention: per-warp (max, sum) of both heads
+  __align__(16) uint16_t knew[HD];   // attention: the new position's bf16 key and value rows
+  __align__(16) uint16_t vnew[HD];
   float rs[RS_MAX];        // FP8 row scales of this CTA's rows in the current phase
   DLayer lay[MAX_LAYERS];  // the layer table, copied once per launch
   Sched sched;             // this CTA's row ranges and attention unit
@@ -725,6 +728,7 @@ struct Consumer {
           const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
           v[j] = bf16f(bits);
           if (S.uc == p.units - 1) cache[row + lane + 32 * j] = bits;
+          (warp == 2 ? s->knew : s->vnew)[lane + 32 * j] = bits;
         }
       }
       float* dst = warp == 0 ? s->qs[0] : (warp == 1 ? s->qs[1] : (warp == 2 ? s->kn : s->vn));
@@ -738,162 +742,138 @@ struct Consumer {
     mark(30);
     if (s->abort) return false;
     const float scale = 0.08838834764831845f;  // 1/sqrt(128)
-    // ---- scores: a group of 8 lanes per position, 16 dims per lane, both heads at once
-    {
-      const int grp = lane >> 3, gl = lane & 7;
-      float q0[16], q1[16];
+    // Each warp takes a contiguous slice of the unit's positions and runs scores, its own softmax
+    // and P.V over it (flash-decoding within the CTA); one CTA barrier merges the eight partials.
+    const int per = (np + NCW - 1) / NCW;
+    const int ws0 = min(np, warp * per), ws1 = min(np, ws0 + per);
+    auto tile_of = [&](int t) { return ring + (size_t)((n + (t >> 5)) % NSLOT) * SLOT + (t & (KVT - 1)) * (HD * 2); };
+    // ---- scores: four lanes per position, 32 dimensions per lane as four 16-byte chunks; odd
+    // positions start at the other half of the banks, so a quarter warp reads two rows without
+    // conflicts, and each lane keeps the matching q elements of both heads in registers
+    const int pp = lane >> 2, l4 = lane & 3;
+    int ch[4];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        q0[e] = s->qs[0][8 * gl + e];
-        q1[e] = s->qs[1][8 * gl + e];
-        q0[8 + e] = s->qs[0][64 + 8 * gl + e];
-        q1[8 + e] = s->qs[1][64 + 8 * gl + e];
-      }
-      float m0 = -INFINITY, m1 = -INFINITY;
-      for (int t = warp * 4 + grp; t - grp < np; t += NCW * 4) {
-        float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-        if (t < np) {
-          uint4 k0, k1;
-          if (t < S.ncached) {
-            const uint8_t* row = ring + (size_t)((n + t / KVT) % NSLOT) * SLOT + (t % KVT) * HD * 2;
-            k0 = *reinterpret_cast<const uint4*>(row + gl * 16);
-            k1 = *reinterpret_cast<const uint4*>(row + 128 + gl * 16);
-          } else {
-            // the new position: convert the float key to the packed bf16 layout on the fly
-            const float* kr = s->kn;
-            uint32_t w[8];
+    for (int j = 0; j < 4; ++j) ch[j] = (4 * j + l4 + 4 * (pp & 1)) & 15;
+    float q0r[32], q1r[32];
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              w[e] = (__float_as_uint(kr[8 * gl + 2 * e]) >> 16) | (__float_as_uint(kr[8 * gl + 2 * e + 1]) & 0xFFFF0000u);
-              w[4 + e] = (__float_as_uint(kr[64 + 8 * gl + 2 * e]) >> 16) |
-                         (__float_as_uint(kr[64 + 8 * gl + 2 * e + 1]) & 0xFFFF0000u);
-            }
-            k0 = make_uint4(w[0], w[1], w[2], w[3]);
-            k1 = make_uint4(w[4], w[5], w[6], w[7]);
-          }
-          const uint32_t kw[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+    for (int j = 0; j < 4; ++j) {
+      const float4* a = reinterpret_cast<const float4*>(s->qs[0] + 8 * ch[j]);
+      const float4* b = reinterpret_cast<const float4*>(s->qs[1] + 8 * ch[j]);
+      const float4 a0 = a[0], a1 = a[1], b0 = b[0], b1 = b[1];
+      q0r[8 * j + 0] = a0.x, q0r[8 * j + 1] = a0.y, q0r[8 * j + 2] = a0.z, q0r[8 * j + 3] = a0.w;
+      q0r[8 * j + 4] = a1.x, q0r[8 * j + 5] = a1.y, q0r[8 * j + 6] = a1.z, q0r[8 * j + 7] = a1.w;
+      q1r[8 * j + 0] = b0.x, q1r[8 * j + 1] = b0.y, q1r[8 * j + 2] = b0.z, q1r[8 * j + 3] = b0.w;
+      q1r[8 * j + 4] = b1.x, q1r[8 * j + 5] = b1.y, q1r[8 * j + 6] = b1.z, q1r[8 * j + 7] = b1.w;
+    }
+    mark(31);
+    float m0 = -INFINITY, m1 = -INFINITY;
+    for (int tb = ws0; tb < ws1; tb += 8) {
+      const int t = tb + pp;
+      float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+      if (t < ws1) {
+        const uint8_t* row = t < S.ncached ? tile_of(t) : reinterpret_cast<const uint8_t*>(s->knew);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float lo = __uint_as_float(kw[e] << 16), hi = __uint_as_float(kw[e] & 0xFFFF0000u);
-            a0 = fmaf(q0[2 * e], lo, a0);
-            a1 = fmaf(q0[2 * e + 1], hi, a1);
-            b0 = fmaf(q1[2 * e], lo, b0);
-            b1 = fmaf(q1[2 * e + 1], hi, b1);
+        for (int j = 0; j < 4; ++j) {
+          const uint4 kw = *reinterpret_cast<const uint4*>(row + 16 * ch[j]);
+          const uint32_t w4[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
+            a0 = fmaf(q0r[8 * j + 2 * e], lo, a0);
+            a1 = fmaf(q0r[8 * j + 2 * e + 1], hi, a1);
+            b0 = fmaf(q1r[8 * j + 2 * e], lo, b0);
+            b1 = fmaf(q1r[8 * j + 2 * e + 1], hi, b1);
           }
         }
-        float a = a0 + a1, b = b0 + b1;
-#pragma unroll
-        for (int o = 4; o; o >>= 1) {
-          a += __shfl_xor_sync(0xffffffffu, a, o);
-          b += __shfl_xor_sync(0xffffffffu, b, o);
-        }
-        if (t < np) {
-          a *= scale;
-          b *= scale;
-          if (gl == 0) {
-            s->sc[0][t] = a;
-            s->sc[1][t] = b;
-          }
-          m0 = fmaxf(m0, a);
-          m1 = fmaxf(m1, b);
-        }
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-        m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
-      }
-      if (lane == 0) {
-        s->red[warp] = m0;
-        s->red[NCW + warp] = m1;
+      float sa = a0 + a1, sb = b0 + b1;
+      sa += __shfl_xor_sync(0xffffffffu, sa, 1);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+      sa += __shfl_xor_sync(0xffffffffu, sa, 2);
+      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+      if (t < ws1) {
+        sa *= scale;
+        sb *= scale;
+        if (l4 == 0) {
+          s->sc[0][t] = sa;
+          s->sc[1][t] = sb;
+        }
+        m0 = fmaxf(m0, sa);
+        m1 = fmaxf(m1, sb);
       }
     }
-    bar_consumers(NCT);
+    mark(32);
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+    }
     mark(33);
-    // ---- softmax numerators of this chunk and their per-head sums
-    {
-      float M0 = lane < NCW ? s->red[lane] : -INFINITY, M1 = lane < NCW ? s->red[NCW + lane] : -INFINITY;
+    __syncwarp();
+    // ---- the warp's softmax numerators and their sums
+    float l0 = 0.f, l1 = 0.f;
+    for (int t = ws0 + lane; t < ws1; t += 32) {
+      const float e0 = expf(s->sc[0][t] - m0), e1 = expf(s->sc[1][t] - m1);
+      s->sc[0][t] = e0;
+      s->sc[1][t] = e1;
+      l0 += e0;
+      l1 += e1;
+    }
 #pragma unroll
-      for (int o = 8; o; o >>= 1) {
-        M0 = fmaxf(M0, __shfl_xor_sync(0xffffffffu, M0, o));
-        M1 = fmaxf(M1, __shfl_xor_sync(0xffffffffu, M1, o));
-      }
-      M0 = __shfl_sync(0xffffffffu, M0, 0);
-      M1 = __shfl_sync(0xffffffffu, M1, 0);
-      float l0 = 0.f, l1 = 0.f;
-      for (int i = tid; i < 2 * np; i += NCT) {
-        const int h = i >= np, t = h ? i - np : i;
-        const float e = expf(s->sc[h][t] - (h ? M1 : M0));
-        s->sc[h][t] = e;
-        if (h) l1 += e;
-        else l0 += e;
-      }
+    for (int o = 16; o; o >>= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+    }
+    __syncwarp();
+    mark(34);
+    // ---- P.V over the slice: lane holds dimensions 4 lane .. 4 lane + 3 of both heads
+    float o0[4] = {0.f, 0.f, 0.f, 0.f}, o1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+    for (int t = ws0; t < ws1; ++t) {
+      const uint8_t* row = t < S.ncached ? tile_of(t) + SLOT / 2 : reinterpret_cast<const uint8_t*>(s->vnew);
+      const uint2 vw = *reinterpret_cast<const uint2*>(row + 8 * lane);
+      const float p0 = s->sc[0][t], p1 = s->sc[1][t];
+      const float v[4] = {__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xFFFF0000u),
+                          __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xFFFF0000u)};
 #pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-        l1 += __shfl_xor_sync(0xffffffffu, l1, o);
-      }
-      if (lane == 0) {
-        s->red[2 * NCW + warp] = l0;
-        s->red[3 * NCW + warp] = l1;
-      }
-      if (tid == 0) {
-        s->stat[0] = M0;
-        s->stat[1] = M1;
+      for (int i = 0; i < 4; ++i) {
+        o0[i] = fmaf(p0, v[i], o0[i]);
+        o1[i] = fmaf(p1, v[i], o1[i]);
       }
     }
-    bar_consumers(NCT);
-    mark(34);
-    // ---- weighted sum of V: work item (slice, d), positions t = slice (mod 4), both heads
-    for (int wi = tid; wi < 4 * HD; wi += NCT) {
-      const int d = wi & (HD - 1), slice = wi >> 7;
-      float a00 = 0.f, a01 = 0.f, a10 = 0.f, a11 = 0.f;
-      auto vat = [&](int t) {
-        const uint8_t* tile = ring + (size_t)((n + t / KVT) % NSLOT) * SLOT;
-        return bf16f(*reinterpret_cast<const uint16_t*>(tile + SLOT / 2 + (t % KVT) * HD * 2 + d * 2));
-      };
-      int t = slice;
-      for (; t + 4 < S.ncached; t += 8) {  // two positions per iteration, independent chains
-        const float v0 = vat(t), v1 = vat(t + 4);
-        a00 = fmaf(s->sc[0][t], v0, a00);
-        a10 = fmaf(s->sc[1][t], v0, a10);
-        a01 = fmaf(s->sc[0][t + 4], v1, a01);
-        a11 = fmaf(s->sc[1][t + 4], v1, a11);
-      }
-      for (; t < S.ncached; t += 4) {
-        const float v0 = vat(t);
-        a00 = fmaf(s->sc[0][t], v0, a00);
-        a10 = fmaf(s->sc[1][t], v0, a10);
-      }
-      if (np > S.ncached && ((np - 1) & 3) == slice) {  // the new position (held in vn)
-        const float v0 = s->vn[d];
-        a01 = fmaf(s->sc[0][np - 1], v0, a01);
-        a11 = fmaf(s->sc[1][np - 1], v0, a11);
-      }
-      float* xsum = s->xs;  // free during attention
-      xsum[(slice * 2 + 0) * HD + d] = a00 + a01;
-      xsum[(slice * 2 + 1) * HD + d] = a10 + a11;
+    float* wo = s->xs;  // [NCW][2][HD] partial outputs (xs is free during attention)
+    *reinterpret_cast<float4*>(wo + (warp * 2 + 0) * HD + 4 * lane) = make_float4(o0[0], o0[1], o0[2], o0[3]);
+    *reinterpret_cast<float4*>(wo + (warp * 2 + 1) * HD + 4 * lane) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+    if (lane == 0) {
+      s->wst[warp][0] = m0;
+      s->wst[warp][1] = m1;
+      s->wst[warp][2] = l0;
+      s->wst[warp][3] = l1;
     }
     bar_consumers(NCT);
     mark(35);
     release_tiles(0, ntiles);
     n += ntiles;
+    // ---- merge the warps (an empty slice has max -inf and sum 0, so its weight is 0)
     if (tid < 2 * HD) {
       const int h = tid / HD, d = tid % HD;
-      const float* xsum = s->xs;
-      const float acc = (xsum[(0 * 2 + h) * HD + d] + xsum[(1 * 2 + h) * HD + d]) +
-                        (xsum[(2 * 2 + h) * HD + d] + xsum[(3 * 2 + h) * HD + d]);
-      float lsum = lane < NCW ? s->red[(2 + h) * NCW + lane] : 0.f;
+      float M = -INFINITY;
 #pragma unroll
-      for (int o = 8; o; o >>= 1) lsum += __shfl_xor_sync(0xffffffffu, lsum, o);
-      lsum = __shfl_sync(0xffffffffu, lsum, 0);
+      for (int w = 0; w < NCW; ++w) M = fmaxf(M, s->wst[w][h]);
+      float lsum = 0.f, acc = 0.f;
+#pragma unroll
+      for (int w = 0; w < NCW; ++w) {
+        const float f = expf(s->wst[w][h] - M);
+        lsum = fmaf(f, s->wst[w][2 + h], lsum);
+        acc = fmaf(f, wo[(w * 2 + h) * HD + d], acc);
+      }
       if (p.units == 1) {  // one unit covers the whole context: no merge needed
         if (!faulted(PH_ATTN, l)) ll_store(p.att + GQA * HD * g + tid, tag, acc / lsum);
       } else {
         float* part = p.attp + (((size_t)g * MAXC + S.uc) * 2 + h) * PART_STRIDE;
         part[4 + d] = acc;
         if (d == 0) {
-          part[0] = s->stat[h];
+          part[0] = M;
           part[1] = lsum;
         }
       }
