@@ -55,7 +55,7 @@ typedef struct {
 
 /* Model shape. This build supports the Qwen3-0.6B shape family: hidden 1024, 16 query heads,
  * 8 KV heads of width 128, FFN 3072 (model bullet, monolith page, "Upstream facts"); any
- * 1 <= n_layers <= 64, 1 <= vocab < 2^24, 1 <= max_ctx <= mk_max_context(). */
+ * 1 <= n_layers <= 40, 1 <= vocab < 2^24, 1 <= max_ctx <= mk_max_context(). */
 typedef struct {
   int n_layers, hidden, n_q_heads, n_kv_heads, head_dim, ffn, vocab, max_ctx;
   float rope_theta; /* 1e6 for Qwen3 */
@@ -188,7 +188,7 @@ int mk_probe_cvt(uint32_t* f16_from_e4m3_dev, uint32_t* f16_from_e2m1_dev, const
  * token in *next_token_host (and the fp32 logits in logits_dev if not NULL).
  * The kernel's scratch (sync words, activation exchange buffers, attention partials, layer table
  * and RoPE table, about 2.6 MB) lives in one fixed device array that every GPU loading the library
- * holds until the process exits; cfg->max_ctx <= MK_STATIC_MAX_CTX and n_layers <= 64.
+ * holds until the process exits; cfg->max_ctx <= MK_STATIC_MAX_CTX and n_layers <= 40.
  * The first call on a device looks the array up on that device (the device must be current), and
  * a call with a new rope_theta rebuilds its RoPE table. Calls share the array: two calls that run
  * at the same time on one GPU race and give wrong results. Synchronises `stream`. Errors:

@@ -144,7 +144,7 @@ int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes
   if (!c || !w || !w->layers) return set_err(nullptr, MK_EINVAL, "config or weights NULL");
   if (c->hidden != HID || c->n_q_heads != NQH || c->n_kv_heads != NKVH || c->head_dim != HD || c->ffn != FFN)
     return set_err(nullptr, MK_EINVAL, "only the Qwen3-0.6B shape family (1024/16/8/128/3072) is supported");
-  if (c->n_layers < 1 || c->n_layers > 64 || c->vocab < 1 || c->vocab >= (1 << 24) || c->max_ctx < 1)
+  if (c->n_layers < 1 || c->n_layers > MAX_LAYERS || c->vocab < 1 || c->vocab >= (1 << 24) || c->max_ctx < 1)
     return set_err(nullptr, MK_EINVAL, "bad n_layers/vocab/max_ctx");
   if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return set_err(nullptr, MK_EINVAL, "bad eps/theta");
   int grid;

@@ -22,7 +22,8 @@ constexpr int NTHREADS = NCT + 32;
 
 // Shared-memory weight ring.
 constexpr int SLOT = 16384;
-constexpr int NSLOT = 11;
+constexpr int NSLOT = 12;
+constexpr int MAX_LAYERS = 40;  // layer table held in each CTA's shared memory
 constexpr int KVT = 32;                         // positions per KV tile (K 8 KB + V 8 KB)
 constexpr int UNIT_TILES = 9;                   // KV tiles an attention unit holds at once
 constexpr int UNIT_POS = KVT * UNIT_TILES;      // 288 positions per attention unit

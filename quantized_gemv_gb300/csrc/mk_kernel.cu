@@ -76,8 +76,7 @@ struct Sched {
   }
 };
 
-constexpr int MAX_LAYERS = 64;
-constexpr int RS_MAX = 3 * NCT;
+constexpr int RS_MAX = NCT;
 struct __align__(16) Smem {
   uint64_t full[NSLOT];
   uint64_t empty[NSLOT];
@@ -187,10 +186,9 @@ struct Producer {
       uint32_t par = ((n / NSLOT) - 1) & 1;
       if (!mbar_test_wait(&s->empty[slot], par)) {
         uint64_t t0 = globaltimer();
-        while (!mbar_test_wait(&s->empty[slot], par)) {
-#ifndef MKX_NOSLEEP
-          __nanosleep(256);  // the ring is full: leave the issue slots to the consumer warps
-#endif
+        // the ring is full: try_wait suspends the warp in hardware (leaving the issue slots to the
+        // consumers) and resumes it as soon as the slot is released
+        while (!mbar_try_wait(&s->empty[slot], par)) {
           if (s->abort) return false;
           if (globaltimer() - t0 > deadline_ns) return false;
         }
@@ -1003,20 +1001,16 @@ struct Consumer {
         // ---- loads that do not depend on this step go out before the wait
         const int nsc = paired ? 2 * nrows : nrows;
         const bool use_rs = fmt == 1 && nsc <= RS_MAX;
-        float sc0 = 0.f, sc1 = 0.f, sc2 = 0.f;
+        float sc0 = 0.f;
         if (use_rs) {
           const float* sa = reinterpret_cast<const float*>(ma.scale) + r0;
           const float* sb = reinterpret_cast<const float*>(mb.scale) + r0;
           auto ld = [&](int v) { return v < nrows ? __ldg(sa + v) : __ldg(sb + (v - nrows)); };
           if (tid < nsc) sc0 = ld(tid);
-          if (tid + NCT < nsc) sc1 = ld(tid + NCT);
-          if (tid + 2 * NCT < nsc) sc2 = ld(tid + 2 * NCT);
         }
         auto store_sc = [&] {
           if (use_rs) {
             if (tid < nsc) rs[tid] = sc0;
-            if (tid + NCT < nsc) rs[tid + NCT] = sc1;
-            if (tid + 2 * NCT < nsc) rs[tid + 2 * NCT] = sc2;
           }
         };
         uint2 wb = make_uint2(0u, 0u);

@@ -24,7 +24,7 @@ using namespace mk;
 
 namespace {
 
-constexpr int STATIC_MAX_LAYERS = 64;
+constexpr int STATIC_MAX_LAYERS = MAX_LAYERS;
 constexpr int STATIC_MAX_CTX = MK_STATIC_MAX_CTX;
 
 struct __align__(256) StaticScratch {
