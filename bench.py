@@ -235,8 +235,7 @@ def time_e2e(model, first: int, pos0: int, k: int):
 
 
 def stream_read_gbs(mk):
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    unit = 16384 * sms
+    unit = 16384 * mk.decode_grid()
     n = (2 << 30) // unit * unit
     buf = torch.empty(n, dtype=torch.uint8, device="cuda")
     for _ in range(3):

@@ -88,6 +88,10 @@ typedef struct mk_model mk_model; /* opaque; library-owned host object */
  * at most one unit per SM, each holding up to 288 positions in shared memory). */
 int mk_max_context(void);
 
+/* CTAs of the persistent decode grid on the current device (one per SM, at most 128), or 0 when
+ * the device cannot be queried. mk_gemv and mk_stream_read use the same grid. */
+int mk_decode_grid(void);
+
 /* Bytes of device workspace a model needs: bf16 KV cache [n_layers][n_kv][max_ctx][head_dim] for
  * keys and for values, a RoPE cos/sin table, activations, sync counters, an optional per-layer
  * hidden-state buffer and, with MK_FLAG_XRAY, the trace buffer. Returns 0 on a bad config. */
@@ -162,7 +166,7 @@ int mk_pack_nvfp4(const void* w_bf16_dev, int rows, int cols, void* codes_dev, v
  * x_dev: fp32 [cols]; y_dev: fp32 [rows]; cols a multiple of 1024 and at most 4096. */
 int mk_gemv(const mk_mat* w, int rows, int cols, const float* x_dev, float* y_dev, void* stream);
 
-/* Streaming-read probe: read `bytes` (multiple of 16 * 1024 * number of SMs) from buf_dev once
+/* Streaming-read probe: read `bytes` (multiple of 16 * 1024 * mk_decode_grid()) from buf_dev once
  * with bulk copies into shared memory, on `stream`. Used to measure achievable HBM bandwidth. */
 int mk_stream_read(const void* buf_dev, size_t bytes, void* stream);
 

@@ -121,6 +121,11 @@ static DMat to_dmat(const mk_mat& m) {
 
 extern "C" {
 
+int mk_decode_grid(void) {
+  int grid;
+  return device_grid(&grid) ? 0 : grid;
+}
+
 int mk_max_context(void) {
   int grid;
   if (device_grid(&grid)) return 0;

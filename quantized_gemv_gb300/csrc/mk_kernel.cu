@@ -325,6 +325,7 @@ struct Consumer {
   // going to the next CTA barrier, where the abort is seen by every warp).
   __device__ void wait_full(uint32_t slot, uint32_t par, int phase, int layer) {
     if (mbar_test_wait(&s->full[slot], par)) return;
+    if (XR && lane == 0 && warp == 0) xr.stamp(54, 4);
     uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s->full[slot], par)) {  // suspends the warp for a while in hardware
       if (s->abort) return;
@@ -573,8 +574,10 @@ struct Consumer {
         const int glast = min(g0 + UPG, nrows) - 1;
         const int ta = TPU * (int)__umulhi((uint32_t)g0, rmag);
         const int tb = TPU * (int)__umulhi((uint32_t)glast, rmag) + TPU - 1;
+        mark(56);
         flush_tiles(released, ta);
         warp_wait_tiles(ta, tb - ta + 1, PH_WAIT, -1);
+        mark(50);
         const uint8_t* code[NR];
         const uint8_t* bsc[NR];
         float sc[NR];
@@ -597,7 +600,9 @@ struct Consumer {
           }
         }
         float part[NR];
+        mark(57);
         dot_rows<FMT, REGX, NR>(code, bsc, nchunk, xr, part);
+        mark(51);
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
 #pragma unroll
@@ -1028,6 +1033,7 @@ struct Consumer {
         }
         st(phase, 0);
         if (normed) e.inv = rms_inv();
+        mark(55);
         gemv(paired, ma, mb, r0, r1, K, use_rs ? rs : nullptr, e);
         bar_consumers(NCT);  // every warp is done with xs, hs and rs before they are restaged
         st(phase, 1);

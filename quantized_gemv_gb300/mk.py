@@ -51,7 +51,7 @@ class mk_weights(C.Structure):
 
 
 # every symbol include/mk.h declares
-EXPORTS = ("mk_max_context", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
+EXPORTS = ("mk_max_context", "mk_decode_grid", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
            "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
            "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
            "mk_decode_step_static")
@@ -66,6 +66,7 @@ def lib():
         L = C.CDLL(path)
         vp, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
         L.mk_max_context.restype = C.c_int
+        L.mk_decode_grid.restype = C.c_int
         L.mk_workspace_bytes.restype = sz
         L.mk_workspace_bytes.argtypes = [C.POINTER(mk_config), C.c_uint]
         L.mk_create.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), vp, sz, vp, C.c_uint, C.POINTER(vp)]
@@ -187,6 +188,10 @@ def probe_cvt(x_f32: torch.Tensor | None = None, stream=None):
 
 def max_context() -> int:
     return lib().mk_max_context()
+
+
+def decode_grid() -> int:
+    return lib().mk_decode_grid()
 
 
 # ------------------------------------------------------------------ the model
