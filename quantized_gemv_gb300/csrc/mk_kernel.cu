@@ -76,7 +76,6 @@ struct Sched {
   }
 };
 
-constexpr int RS_MAX = NCT;
 struct __align__(16) Smem {
   uint64_t full[NSLOT];
   uint64_t empty[NSLOT];
@@ -93,7 +92,6 @@ struct __align__(16) Smem {
   float wst[NCW][4];                 // attention: per-warp (max, sum) of both heads
   __align__(16) uint16_t knew[HD];   // attention: the new position's bf16 key and value rows
   __align__(16) uint16_t vnew[HD];
-  float rs[RS_MAX];        // FP8 row scales of this CTA's rows in the current phase
   DLayer lay[MAX_LAYERS];  // the layer table, copied once per launch
   Sched sched;             // this CTA's row ranges and attention unit
   int flag;
@@ -325,7 +323,7 @@ struct Consumer {
   // going to the next CTA barrier, where the abort is seen by every warp).
   __device__ void wait_full(uint32_t slot, uint32_t par, int phase, int layer) {
     if (mbar_test_wait(&s->full[slot], par)) return;
-    if (XR && lane == 0 && warp == 0) xr.stamp(54, 4);
+    if (XR && warp == 0 && lane == 0) xr.stamp(54, 4);  // X-ray: a tile was not there yet
     uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s->full[slot], par)) {  // suspends the warp for a while in hardware
       if (s->abort) return;
@@ -546,8 +544,60 @@ struct Consumer {
       released += c;
     }
   }
+  // ---------------------------------------------------------------- phase plan
+  // The row-group width of a phase: six rows (three FFN units, gate and up) for gate/up, four rows
+  // for K = 1024, one row a warp for short phases of longer rows, else four.
+  __device__ __forceinline__ static int group_rows(bool paired, int K, int nrows) {
+    return paired ? 6 : (K == 1024 ? 4 : (nrows <= NCW ? 1 : 4));
+  }
+  // Rows per tile and the umulhi magic for a runtime (format, K): compile-time constants behind a
+  // switch, so the hot path has no integer division.
+  __device__ __forceinline__ static void geom_rt(int fmt, int K, int& rpt, uint32_t& mag) {
+    if (fmt == 0) geom_of<0>(K, rpt, mag);
+    else if (fmt == 1) geom_of<1>(K, rpt, mag);
+    else geom_of<2>(K, rpt, mag);
+  }
+  // This warp's first row group of a GEMV phase, prepared before the phase's input arrives: its
+  // row pointers into the ring and its row scales (their loads overlap the wait). The tiles are
+  // waited for, and the ones before the group released, by the engine after the input arrived.
+  struct Plan {
+    const uint8_t* code[6];
+    const uint8_t* bsc[6];
+    float sc[6];
+  };
+  __device__ void plan_first(bool paired, const DMat& ma, const DMat& mb, int r0, int r1, int K, Plan& pl) {
+    const int nrows = r1 - r0;
+    const int NR = group_rows(paired, K, nrows);
+    const int UPG = paired ? NR / 2 : NR, TPU = paired ? 2 : 1;
+    const int g0 = UPG * warp;
+    if (nrows <= 0 || g0 >= nrows) return;
+    const int fmt = ma.fmt;
+    const int cb = code_bytes(fmt, K), sbytes = scale_bytes(fmt, K);
+    int rpt;
+    uint32_t rmag;
+    geom_rt(fmt, K, rpt, rmag);
+    const int T = (int)__umulhi((uint32_t)(nrows + rpt - 1), rmag);
+    const float* sca = reinterpret_cast<const float*>(ma.scale) + r0;
+    const float* scb = reinterpret_cast<const float*>(mb.scale) + r0;
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+      if (k < NR) {
+        const int u = g0 + (paired ? (k >> 1) : k);
+        const bool isb = paired && (k & 1);
+        const int uu = u < nrows ? u : g0;
+        const int tl = (int)__umulhi((uint32_t)uu, rmag);
+        const int rit = uu - tl * rpt;
+        const int nr = tl == T - 1 ? nrows - tl * rpt : rpt;
+        const uint8_t* tile = ring + (size_t)((n + TPU * tl + (isb ? 1 : 0)) % NSLOT) * SLOT;
+        pl.code[k] = tile + (size_t)rit * cb;
+        pl.bsc[k] = tile + (size_t)nr * cb + (size_t)rit * sbytes;
+        pl.sc[k] = fmt == 1 ? __ldg((isb ? scb : sca) + uu) : (fmt == 2 ? (isb ? mb.tscale : ma.tscale) : 1.f);
+      }
+    }
+  }
+
   template <int FMT, bool REGX, bool PAIRED, int NR>
-  __device__ void gemv_t(const DMat& ma, const DMat& mb, int r0, int r1, int K, const float* srow, const EpiCtx& e) {
+  __device__ void gemv_t(const DMat& ma, const DMat& mb, int r0, int r1, int K, const Plan& pl, const EpiCtx& e) {
     constexpr int EPL = FMT == 0 ? 8 : (FMT == 1 ? 16 : 32);
     constexpr int UPG = PAIRED ? NR / 2 : NR;  // units per group
     constexpr int TPU = PAIRED ? 2 : 1;        // tiles per block of rpt units
@@ -571,38 +621,38 @@ struct Consumer {
     for (int b0 = 0; b0 < nrows; b0 += UPG * NCW) {
       const int g0 = b0 + UPG * warp;
       if (g0 < nrows) {
-        const int glast = min(g0 + UPG, nrows) - 1;
-        const int ta = TPU * (int)__umulhi((uint32_t)g0, rmag);
-        const int tb = TPU * (int)__umulhi((uint32_t)glast, rmag) + TPU - 1;
-        mark(56);
-        flush_tiles(released, ta);
-        warp_wait_tiles(ta, tb - ta + 1, PH_WAIT, -1);
-        mark(50);
         const uint8_t* code[NR];
         const uint8_t* bsc[NR];
         float sc[NR];
+        const int glast = min(g0 + UPG, nrows) - 1;
+        const int ta = TPU * (int)__umulhi((uint32_t)g0, rmag);
+        const int tb = TPU * (int)__umulhi((uint32_t)glast, rmag) + TPU - 1;
+        flush_tiles(released, ta);
+        warp_wait_tiles(ta, tb - ta + 1, PH_WAIT, -1);
+        if (b0 == 0) {  // the first group was prepared before the input arrived
 #pragma unroll
-        for (int k = 0; k < NR; ++k) {
-          const int u = g0 + (PAIRED ? (k >> 1) : k);
-          const bool isb = PAIRED && (k & 1);
-          const int uu = u < nrows ? u : g0;
-          const int tl = (int)__umulhi((uint32_t)uu, rmag);
-          const int rit = uu - tl * rpt;
-          const int nr = tl == T - 1 ? nrows - tl * rpt : rpt;
-          const uint8_t* tile = ring + (size_t)((n + TPU * tl + (isb ? 1 : 0)) % NSLOT) * SLOT;
-          code[k] = tile + (size_t)rit * cb;
-          bsc[k] = tile + (size_t)nr * cb + (size_t)rit * sbytes;
-          if constexpr (FMT == 1) {
-            const int si = isb ? nrows + uu : uu;
-            sc[k] = srow ? srow[si] : __ldg((isb ? scb : sca) + uu);
-          } else {
-            sc[k] = FMT == 2 ? (isb ? mb.tscale : ma.tscale) : 1.f;
+          for (int k = 0; k < NR; ++k) code[k] = pl.code[k], bsc[k] = pl.bsc[k], sc[k] = pl.sc[k];
+        } else {
+#pragma unroll
+          for (int k = 0; k < NR; ++k) {
+            const int u = g0 + (PAIRED ? (k >> 1) : k);
+            const bool isb = PAIRED && (k & 1);
+            const int uu = u < nrows ? u : g0;
+            const int tl = (int)__umulhi((uint32_t)uu, rmag);
+            const int rit = uu - tl * rpt;
+            const int nr = tl == T - 1 ? nrows - tl * rpt : rpt;
+            const uint8_t* tile = ring + (size_t)((n + TPU * tl + (isb ? 1 : 0)) % NSLOT) * SLOT;
+            code[k] = tile + (size_t)rit * cb;
+            bsc[k] = tile + (size_t)nr * cb + (size_t)rit * sbytes;
+            if constexpr (FMT == 1) {
+              sc[k] = __ldg((isb ? scb : sca) + uu);
+            } else {
+              sc[k] = FMT == 2 ? (isb ? mb.tscale : ma.tscale) : 1.f;
+            }
           }
         }
         float part[NR];
-        mark(57);
         dot_rows<FMT, REGX, NR>(code, bsc, nchunk, xr, part);
-        mark(51);
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
 #pragma unroll
@@ -631,28 +681,28 @@ struct Consumer {
     }
     n += ntiles;
   }
-  // Dispatch on format and width (the one call site of the engine).
-  __device__ void gemv(bool paired, const DMat& ma, const DMat& mb, int r0, int r1, int K, const float* srow,
+  // Dispatch on format and group width (the one call site of the engine).
+  __device__ void gemv(bool paired, const DMat& ma, const DMat& mb, int r0, int r1, int K, const Plan& pl,
                        const EpiCtx& e) {
     if (r0 >= r1) return;
     const int fmt = ma.fmt;
-    const bool one = r1 - r0 <= NCW;  // at most one row per warp: one row per pass
+    const int nr = group_rows(paired, K, r1 - r0);
     if (paired) {
-      if (fmt == 0) gemv_t<0, true, true, 6>(ma, mb, r0, r1, K, srow, e);
-      else if (fmt == 1) gemv_t<1, true, true, 6>(ma, mb, r0, r1, K, srow, e);
-      else gemv_t<2, true, true, 6>(ma, mb, r0, r1, K, srow, e);
+      if (fmt == 0) gemv_t<0, true, true, 6>(ma, mb, r0, r1, K, pl, e);
+      else if (fmt == 1) gemv_t<1, true, true, 6>(ma, mb, r0, r1, K, pl, e);
+      else gemv_t<2, true, true, 6>(ma, mb, r0, r1, K, pl, e);
     } else if (K == 1024) {
-      if (fmt == 0) gemv_t<0, true, false, 4>(ma, mb, r0, r1, K, srow, e);
-      else if (fmt == 1) gemv_t<1, true, false, 4>(ma, mb, r0, r1, K, srow, e);
-      else gemv_t<2, true, false, 4>(ma, mb, r0, r1, K, srow, e);
-    } else if (one) {
-      if (fmt == 0) gemv_t<0, false, false, 1>(ma, mb, r0, r1, K, srow, e);
-      else if (fmt == 1) gemv_t<1, false, false, 1>(ma, mb, r0, r1, K, srow, e);
-      else gemv_t<2, false, false, 1>(ma, mb, r0, r1, K, srow, e);
+      if (fmt == 0) gemv_t<0, true, false, 4>(ma, mb, r0, r1, K, pl, e);
+      else if (fmt == 1) gemv_t<1, true, false, 4>(ma, mb, r0, r1, K, pl, e);
+      else gemv_t<2, true, false, 4>(ma, mb, r0, r1, K, pl, e);
+    } else if (nr == 1) {
+      if (fmt == 0) gemv_t<0, false, false, 1>(ma, mb, r0, r1, K, pl, e);
+      else if (fmt == 1) gemv_t<1, false, false, 1>(ma, mb, r0, r1, K, pl, e);
+      else gemv_t<2, false, false, 1>(ma, mb, r0, r1, K, pl, e);
     } else {
-      if (fmt == 0) gemv_t<0, false, false, 4>(ma, mb, r0, r1, K, srow, e);
-      else if (fmt == 1) gemv_t<1, false, false, 4>(ma, mb, r0, r1, K, srow, e);
-      else gemv_t<2, false, false, 4>(ma, mb, r0, r1, K, srow, e);
+      if (fmt == 0) gemv_t<0, false, false, 4>(ma, mb, r0, r1, K, pl, e);
+      else if (fmt == 1) gemv_t<1, false, false, 4>(ma, mb, r0, r1, K, pl, e);
+      else gemv_t<2, false, false, 4>(ma, mb, r0, r1, K, pl, e);
     }
   }
 
@@ -942,7 +992,6 @@ struct Consumer {
     }
     bar_consumers(NCT);
     st(PH_EMBED, 1);
-    float* rs = s->rs;
     best = -INFINITY;
     besti = 0x7FFFFFFF;
     // One pass per (layer, step); the single GEMV and wait call sites keep one code copy each.
@@ -1002,22 +1051,10 @@ struct Consumer {
         }
         if (!paired) mb = ma;
         const int fmt = ma.fmt;
-        const int nrows = r1 - r0;
-        // ---- loads that do not depend on this step go out before the wait
-        const int nsc = paired ? 2 * nrows : nrows;
-        const bool use_rs = fmt == 1 && nsc <= RS_MAX;
-        float sc0 = 0.f;
-        if (use_rs) {
-          const float* sa = reinterpret_cast<const float*>(ma.scale) + r0;
-          const float* sb = reinterpret_cast<const float*>(mb.scale) + r0;
-          auto ld = [&](int v) { return v < nrows ? __ldg(sa + v) : __ldg(sb + (v - nrows)); };
-          if (tid < nsc) sc0 = ld(tid);
-        }
-        auto store_sc = [&] {
-          if (use_rs) {
-            if (tid < nsc) rs[tid] = sc0;
-          }
-        };
+        // ---- everything that does not depend on this step's input happens before the wait:
+        // this warp's first row group (tiles, row pointers, row scales) and the norm weights
+        Plan pl;
+        if (r0 < r1) plan_first(paired, ma, mb, r0, r1, K, pl);
         uint2 wb = make_uint2(0u, 0u);
         if (normed) {
           wb.x = __ldg(reinterpret_cast<const uint32_t*>(nw) + tid);
@@ -1025,17 +1062,15 @@ struct Consumer {
         }
         if (step == ST_QKV && l == 0) {  // the input is the embedding row already in hs
           stage_local(wb, fmt);
-          store_sc();
           bar_consumers(NCT);
         } else if (!poll_stage(src, nsrc, stag, phase == PH_QKV || phase == PH_HEAD ? PH_DOWN : phase - 1, l,
-                               normed, wb, fmt, store_sc)) {
+                               normed, wb, fmt, [] {})) {
           return;
         }
         st(phase, 0);
         if (normed) e.inv = rms_inv();
-        mark(55);
-        gemv(paired, ma, mb, r0, r1, K, use_rs ? rs : nullptr, e);
-        bar_consumers(NCT);  // every warp is done with xs, hs and rs before they are restaged
+        gemv(paired, ma, mb, r0, r1, K, pl, e);
+        bar_consumers(NCT);  // every warp is done with xs and hs before they are restaged
         st(phase, 1);
       }
     }
@@ -1170,7 +1205,9 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
     e.ll = nullptr;
     e.fout = y;
     e.dbg = nullptr;
-    c.gemv(false, m, m, r0, r1, cols, nullptr, e);
+    typename Consumer<false>::Plan pl;
+    if (r0 < r1) c.plan_first(false, m, m, r0, r1, cols, pl);
+    c.gemv(false, m, m, r0, r1, cols, pl, e);
     bar_consumers(NCT);
   }
 }
