@@ -46,6 +46,7 @@ struct Sched {
   int v0, v1;    // LM-head rows
   bool unit;     // this CTA runs an attention unit
   int ug, uc;    // its KV head and chunk
+  int hq;        // single-head unit: which q head of the KV group (0 or 1); -1: both heads
   int t0, t1;    // positions [t0, t1) of the chunk
   int ncached;   // positions of the chunk already in the cache (read through the ring)
   __device__ void make(const KParams& P) {
@@ -67,9 +68,17 @@ struct Sched {
     split_range(FFN, G, b, j0, j1);
     split_range(HID, G, b, d0, d1);
     split_range(P.vocab, G, b, v0, v1);
-    unit = b < NKVH * P.units;
-    ug = unit ? b / P.units : 0;
-    uc = unit ? b % P.units : 0;
+    if (P.units == 1) {  // the whole context fits one unit: one unit per q head (16 CTAs)
+      unit = b < NQH;
+      ug = unit ? b / GQA : 0;
+      hq = unit ? b % GQA : 0;
+      uc = 0;
+    } else {             // position chunks of every KV head, both q heads per unit
+      unit = b < NKVH * P.units;
+      ug = unit ? b / P.units : 0;
+      uc = unit ? b % P.units : 0;
+      hq = -1;
+    }
     split_range(P.pos + 1, P.units, uc, t0, t1);
     int c_end = t1 < P.pos ? t1 : P.pos;
     ncached = unit ? (c_end > t0 ? c_end - t0 : 0) : 0;
@@ -706,14 +715,18 @@ struct Consumer {
     }
   }
 
-  // One attention unit: KV head g, positions [S.t0, S.t1) of layer l.
+  // One attention unit: KV head g, positions [S.t0, S.t1) of layer l; q head 2g + S.hq alone
+  // (S.hq >= 0) or both q heads of the group.
   __device__ bool attention(const Sched& S, const DLayer& L, int l, uint32_t tag) {
     const KParams& p = *P;
     const int g = S.ug;
-    // Warps 0..3 own one 128-wide vector each (q of head 2g, q of head 2g+1, k, v); lane holds
-    // elements lane + 32 j, so RoPE pairs (i, i + 64) stay in one lane and QK-norm is a shuffle.
-    if (warp < 4) {
-      const int src = warp < 2 ? GQA * HD * g + warp * HD : (warp == 2 ? QROWS + HD * g : QROWS + KVROWS + HD * g);
+    const bool both = S.hq < 0;
+    // Warps 0..3 own one 128-wide vector each (q of the unit's first head, q of head 2g+1 when the
+    // unit has both, k, v); lane holds elements lane + 32 j, so RoPE pairs (i, i + 64) stay in one
+    // lane and QK-norm is a shuffle.
+    if (warp < 4 && (warp != 1 || both)) {
+      const int qh = warp == 0 ? (both ? 0 : S.hq) : 1;
+      const int src = warp < 2 ? GQA * HD * g + qh * HD : (warp == 2 ? QROWS + HD * g : QROWS + KVROWS + HD * g);
       // loads that do not depend on this step's data go out before the wait
       float nw[4] = {1.f, 1.f, 1.f, 1.f}, rc[2], rsn[2];
       if (warp < 3) {
@@ -780,7 +793,7 @@ struct Consumer {
         for (int j = 0; j < 4; ++j) {
           const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
           v[j] = bf16f(bits);
-          if (S.uc == p.units - 1) cache[row + lane + 32 * j] = bits;
+          if (S.uc == p.units - 1 && S.hq <= 0) cache[row + lane + 32 * j] = bits;
           (warp == 2 ? s->knew : s->vnew)[lane + 32 * j] = bits;
         }
       }
@@ -794,6 +807,15 @@ struct Consumer {
     bar_consumers(NCT);
     mark(30);
     if (s->abort) return false;
+    return both ? attn_core<2>(S, l, tag, np, ntiles) : attn_core<1>(S, l, tag, np, ntiles);
+  }
+
+  // Scores, softmax and P.V of an attention unit over its positions for HEADS q heads (q in qs,
+  // the new key and value in knew / vnew, the cached ones in the ring), then its output.
+  template <int HEADS>
+  __device__ bool attn_core(const Sched& S, int l, uint32_t tag, int np, int ntiles) {
+    const KParams& p = *P;
+    const int g = S.ug;
     const float scale = 0.08838834764831845f;  // 1/sqrt(128)
     // Each warp takes a contiguous slice of the unit's positions and runs scores, its own softmax
     // and P.V over it (flash-decoding within the CTA); one CTA barrier merges the eight partials.
@@ -811,12 +833,15 @@ struct Consumer {
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float4* a = reinterpret_cast<const float4*>(s->qs[0] + 8 * ch[j]);
-      const float4* b = reinterpret_cast<const float4*>(s->qs[1] + 8 * ch[j]);
-      const float4 a0 = a[0], a1 = a[1], b0 = b[0], b1 = b[1];
+      const float4 a0 = a[0], a1 = a[1];
       q0r[8 * j + 0] = a0.x, q0r[8 * j + 1] = a0.y, q0r[8 * j + 2] = a0.z, q0r[8 * j + 3] = a0.w;
       q0r[8 * j + 4] = a1.x, q0r[8 * j + 5] = a1.y, q0r[8 * j + 6] = a1.z, q0r[8 * j + 7] = a1.w;
-      q1r[8 * j + 0] = b0.x, q1r[8 * j + 1] = b0.y, q1r[8 * j + 2] = b0.z, q1r[8 * j + 3] = b0.w;
-      q1r[8 * j + 4] = b1.x, q1r[8 * j + 5] = b1.y, q1r[8 * j + 6] = b1.z, q1r[8 * j + 7] = b1.w;
+      if constexpr (HEADS == 2) {
+        const float4* b = reinterpret_cast<const float4*>(s->qs[1] + 8 * ch[j]);
+        const float4 b0 = b[0], b1 = b[1];
+        q1r[8 * j + 0] = b0.x, q1r[8 * j + 1] = b0.y, q1r[8 * j + 2] = b0.z, q1r[8 * j + 3] = b0.w;
+        q1r[8 * j + 4] = b1.x, q1r[8 * j + 5] = b1.y, q1r[8 * j + 6] = b1.z, q1r[8 * j + 7] = b1.w;
+      }
     }
     mark(31);
     float m0 = -INFINITY, m1 = -INFINITY;
@@ -834,48 +859,55 @@ struct Consumer {
             const float lo = __uint_as_float(w4[e] << 16), hi = __uint_as_float(w4[e] & 0xFFFF0000u);
             a0 = fmaf(q0r[8 * j + 2 * e], lo, a0);
             a1 = fmaf(q0r[8 * j + 2 * e + 1], hi, a1);
-            b0 = fmaf(q1r[8 * j + 2 * e], lo, b0);
-            b1 = fmaf(q1r[8 * j + 2 * e + 1], hi, b1);
+            if constexpr (HEADS == 2) {
+              b0 = fmaf(q1r[8 * j + 2 * e], lo, b0);
+              b1 = fmaf(q1r[8 * j + 2 * e + 1], hi, b1);
+            }
           }
         }
       }
       float sa = a0 + a1, sb = b0 + b1;
       sa += __shfl_xor_sync(0xffffffffu, sa, 1);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 1);
       sa += __shfl_xor_sync(0xffffffffu, sa, 2);
-      sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+      if constexpr (HEADS == 2) {
+        sb += __shfl_xor_sync(0xffffffffu, sb, 1);
+        sb += __shfl_xor_sync(0xffffffffu, sb, 2);
+      }
       if (t < ws1) {
         sa *= scale;
         sb *= scale;
         if (l4 == 0) {
           s->sc[0][t] = sa;
-          s->sc[1][t] = sb;
+          if (HEADS == 2) s->sc[1][t] = sb;
         }
         m0 = fmaxf(m0, sa);
-        m1 = fmaxf(m1, sb);
+        if (HEADS == 2) m1 = fmaxf(m1, sb);
       }
     }
     mark(32);
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
-      m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+      if (HEADS == 2) m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
     }
     mark(33);
     __syncwarp();
     // ---- the warp's softmax numerators and their sums
     float l0 = 0.f, l1 = 0.f;
     for (int t = ws0 + lane; t < ws1; t += 32) {
-      const float e0 = expf(s->sc[0][t] - m0), e1 = expf(s->sc[1][t] - m1);
+      const float e0 = expf(s->sc[0][t] - m0);
       s->sc[0][t] = e0;
-      s->sc[1][t] = e1;
       l0 += e0;
-      l1 += e1;
+      if constexpr (HEADS == 2) {
+        const float e1 = expf(s->sc[1][t] - m1);
+        s->sc[1][t] = e1;
+        l1 += e1;
+      }
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) {
       l0 += __shfl_xor_sync(0xffffffffu, l0, o);
-      l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+      if (HEADS == 2) l1 += __shfl_xor_sync(0xffffffffu, l1, o);
     }
     __syncwarp();
     mark(34);
@@ -885,18 +917,19 @@ struct Consumer {
     for (int t = ws0; t < ws1; ++t) {
       const uint8_t* row = t < S.ncached ? tile_of(t) + SLOT / 2 : reinterpret_cast<const uint8_t*>(s->vnew);
       const uint2 vw = *reinterpret_cast<const uint2*>(row + 8 * lane);
-      const float p0 = s->sc[0][t], p1 = s->sc[1][t];
+      const float p0 = s->sc[0][t], p1 = HEADS == 2 ? s->sc[1][t] : 0.f;
       const float v[4] = {__uint_as_float(vw.x << 16), __uint_as_float(vw.x & 0xFFFF0000u),
                           __uint_as_float(vw.y << 16), __uint_as_float(vw.y & 0xFFFF0000u)};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         o0[i] = fmaf(p0, v[i], o0[i]);
-        o1[i] = fmaf(p1, v[i], o1[i]);
+        if (HEADS == 2) o1[i] = fmaf(p1, v[i], o1[i]);
       }
     }
     float* wo = s->xs;  // [NCW][2][HD] partial outputs (xs is free during attention)
     *reinterpret_cast<float4*>(wo + (warp * 2 + 0) * HD + 4 * lane) = make_float4(o0[0], o0[1], o0[2], o0[3]);
-    *reinterpret_cast<float4*>(wo + (warp * 2 + 1) * HD + 4 * lane) = make_float4(o1[0], o1[1], o1[2], o1[3]);
+    if (HEADS == 2)
+      *reinterpret_cast<float4*>(wo + (warp * 2 + 1) * HD + 4 * lane) = make_float4(o1[0], o1[1], o1[2], o1[3]);
     if (lane == 0) {
       s->wst[warp][0] = m0;
       s->wst[warp][1] = m1;
@@ -908,7 +941,7 @@ struct Consumer {
     release_tiles(0, ntiles);
     n += ntiles;
     // ---- merge the warps (an empty slice has max -inf and sum 0, so its weight is 0)
-    if (tid < 2 * HD) {
+    if (tid < HEADS * HD) {
       const int h = tid / HD, d = tid % HD;
       float M = -INFINITY;
 #pragma unroll
@@ -921,7 +954,8 @@ struct Consumer {
         acc = fmaf(f, wo[(w * 2 + h) * HD + d], acc);
       }
       if (p.units == 1) {  // one unit covers the whole context: no merge needed
-        if (!faulted(PH_ATTN, l)) ll_store(p.att + GQA * HD * g + tid, tag, acc / lsum);
+        const int oh = HEADS == 2 ? h : S.hq;  // q head of the group this output belongs to
+        if (!faulted(PH_ATTN, l)) ll_store(p.att + GQA * HD * g + oh * HD + d, tag, acc / lsum);
       } else {
         float* part = p.attp + (((size_t)g * MAXC + S.uc) * 2 + h) * PART_STRIDE;
         part[4 + d] = acc;
