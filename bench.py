@@ -300,6 +300,19 @@ def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_ste
     return res, master
 
 
+def whole_job_rate(local_total_ms: float, steps: int, world: int, dist=None):
+    """Replicas: tokens of all ranks over the slowest rank's timed region -> (tok/s, that time in ms).
+
+    Every rank calls this (the MAX all-reduce is collective); without a process group it is the
+    single-GPU rate."""
+    total_ms = float(local_total_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return world * steps / (total_ms * 1e-3), total_ms
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -340,13 +353,7 @@ def main():
     from quantized_gemv_gb300 import mk
     stream_gbs = stream_read_gbs(mk) if rank == 0 else None
     res, master = run_workload(wl, args.steps, args.warmup, mk, dist)
-    # whole-job value: tokens of all replicas over the slowest replica's time
-    total_ms = res["ms_per_step"] * args.steps
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = world * args.steps / (total_ms * 1e-3)
+    value, total_ms = whole_job_rate(res["ms_per_step"] * args.steps, args.steps, world, dist)
     peak, peak_kind = measured_peaks()
     achieved = (res["weight_bytes"] + res["kv_bytes"]) / (res["launch_ms"] * 1e-3) / 1e9
     variants = {}
