@@ -123,11 +123,13 @@ class ClockSampler:
             self.ok = False
 
     def read(self):
-        clk, mx, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        clk, mx, rs, mw = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong(), ctypes.c_uint()
         self.nv.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(clk))       # NVML_CLOCK_SM
         self.nv.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx))
         self.nv.nvmlDeviceGetCurrentClocksEventReasons(self.h, ctypes.byref(rs))
-        return clk.value, mx.value, rs.value
+        if self.nv.nvmlDeviceGetPowerUsage(self.h, ctypes.byref(mw)) != 0:  # board power, mW
+            mw.value = 0
+        return clk.value, mx.value, rs.value, mw.value
 
     def __enter__(self):
         self._stop = False
@@ -152,13 +154,18 @@ class ClockSampler:
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvml unavailable"]}
         reasons = set()
-        for _, _, r in self.samples:
+        for _, _, r, _ in self.samples:
             for bit, name in self.REASONS.items():
                 if r & bit and name != "gpu_idle":
                     reasons.add(name)
         return {"sm_mhz": statistics.median(s[0] for s in self.samples),
                 "sm_max_mhz": max(s[1] for s in self.samples), "samples": len(self.samples),
                 "reasons": sorted(reasons)}
+
+    def watts(self):
+        """Median board power over the samples (W), or None."""
+        p = [s[3] for s in self.samples if s[3] > 0]
+        return statistics.median(p) / 1e3 if p else None
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -278,6 +285,67 @@ def oracle_sample(wl: S.Workload, master, seconds: float = 12.0):
                       f"({el:.1f} s, double precision, {cores} threads)"}
 
 
+def xray_summary(wl: S.Workload, mk, master, steps: int = 16):
+    """The same workload through the instrumented build (MK_FLAG_XRAY): the last step's split of a
+    token into weight-read, wait, attention and LM-head time, and the instrumented throughput."""
+    from quantized_gemv_gb300 import xray
+    cfg = wl.config()
+    packed = mk.pack_model(master, S.format_map(wl.variant))
+    model = mk.Model(cfg, packed, flags=mk.MK_FLAG_XRAY)
+    prompt = S.prompt_ids(cfg, wl.prompt_len)
+    tok = int(prompt[0])
+    for pos in range(wl.prompt_len):
+        nxt = model.decode_step(tok, pos)
+        tok = int(prompt[pos + 1]) if pos + 1 < wl.prompt_len else nxt
+    total_ms, _, _ = time_steps(model, tok, wl.prompt_len, steps, 2)
+    a = xray.analyze(model.trace())
+    model.close()
+    t = a["token_ns"]
+    return {"token_us": round(t / 1e3, 1), "ctas": a["ctas"],
+            "weight_read_share": round(a["weight_read_ns"] / t, 3), "barrier_wait_share": round(a["barrier_wait_share"], 3),
+            "attention_share": round(a["attention_ns"] / t, 3), "lm_head_share": round(a["lm_head_ns"] / t, 3),
+            "instrumented_tok_s": round(steps / (total_ms * 1e-3), 1),
+            "note": "one instrumented step at the end of a 16-step greedy run; shares of the token's wall time, "
+                    "averaged over CTAs"}
+
+
+SWEEP_POSITIONS = (16, 128, 512, 1024, 2048)
+
+
+def run_sweep(mk, steps: int = 32, warmup: int = 3):
+    """Decode throughput and energy against context length: the FP8 model with the KV cache prefilled
+    (seeded N(0,1) bf16) to each position, then `steps` greedy steps from there."""
+    import dataclasses
+    base = S.WORKLOADS["qwen3_0.6b_fp8"]
+    cfg = dataclasses.replace(base.config(), max_ctx=max(SWEEP_POSITIONS) + steps + 8)
+    master = S.master_weights(cfg, seed=0)
+    packed = mk.pack_model(master, S.format_map(base.variant))
+    model = mk.Model(cfg, packed)
+    k_all, v_all = S.prefill_kv(cfg, max(SWEEP_POSITIONS), seed=2)
+    for l in range(cfg.n_layers):
+        kt, vt = model.kv_cache(l)
+        kt[:, : max(SWEEP_POSITIONS)].copy_(mk.upload_bf16(k_all[l]))
+        vt[:, : max(SWEEP_POSITIONS)].copy_(mk.upload_bf16(v_all[l]))
+    first = int(S.prompt_ids(cfg, 1)[0])
+    wbytes = weight_bytes(cfg, base.variant)
+    rows = []
+    for p0 in SWEEP_POSITIONS:
+        sampler = ClockSampler(torch.cuda.current_device())
+        with sampler:
+            total_ms, per, _ = time_steps(model, first, p0, steps, warmup)
+        tok_s = steps / (total_ms * 1e-3)
+        w = sampler.watts()
+        kv = kv_bytes(cfg, p0 + (steps - 1) // 2)
+        rows.append({"pos": f"{p0}..{p0 + steps - 1}", "tok_s": round(tok_s, 1), "ms_per_step": round(total_ms / steps, 4),
+                     "gbs_weights_kv": round((wbytes + kv) / (float(np.mean(per)) * 1e-3) / 1e9, 1),
+                     "watts": round(w, 1) if w else None, "tok_per_joule": round(tok_s / w, 2) if w else None,
+                     "clocks": sampler.summary()})
+    model.close()
+    return {"metric": "batch-1 decode tok/s and tokens per joule against context length (Qwen3-0.6B shape, FP8)",
+            "unit": "tok/s", "higher_is_better": True, "steps_per_point": steps, "warmup": warmup,
+            "data": "synthetic (seeded N(0,0.02) weights; KV cache prefilled N(0,1) bf16)", "sweep": rows}
+
+
 def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_steps: int | None = None):
     cfg, master, model, pos0, first = setup_model(wl, mk)
     k = steps
@@ -293,7 +361,7 @@ def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_ste
     res = {"tok_s": k / (total_ms * 1e-3), "ms_per_step": total_ms / k, "launch_ms": launch_ms,
            "weight_bytes": wbytes, "kv_bytes": kv_bytes(cfg, int(round(mean_pos))),
            "e2e_tok_s": (e2e_steps or k) / (e2e_ms * 1e-3), "clocks": sampler.summary(),
-           "first_tokens": toks[:4].tolist()}
+           "watts": sampler.watts(), "first_tokens": toks[:4].tolist()}
     res["weight_gbs"] = wbytes / (launch_ms * 1e-3) / 1e9
     res["total_gbs"] = (wbytes + res["kv_bytes"]) / (launch_ms * 1e-3) / 1e9
     model.close()
@@ -322,6 +390,8 @@ def main():
     ap.add_argument("--impl", default="engine", choices=["engine", "reference"])
     ap.add_argument("--no-variants", action="store_true", help="skip the FP8/NVFP4/long-context lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-xray", action="store_true", help="skip the instrumented-build summary")
+    ap.add_argument("--sweep", action="store_true", help="print the context-length sweep (FP8) instead")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -351,6 +421,10 @@ def main():
 
     torch.cuda.set_device(local)
     from quantized_gemv_gb300 import mk
+    if args.sweep:
+        if rank == 0:
+            print(json.dumps(run_sweep(mk)))
+        return
     stream_gbs = stream_read_gbs(mk) if rank == 0 else None
     res, master = run_workload(wl, args.steps, args.warmup, mk, dist)
     value, total_ms = whole_job_rate(res["ms_per_step"] * args.steps, args.steps, world, dist)
@@ -358,16 +432,20 @@ def main():
     achieved = (res["weight_bytes"] + res["kv_bytes"]) / (res["launch_ms"] * 1e-3) / 1e9
     variants = {}
     if not args.no_variants and rank == 0:
-        for name in ("qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4", "qwen3_0.6b_fp8_ctx4096"):
+        for name in ("qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4", "qwen3_0.6b_fp8_bf16head", "qwen3_0.6b_fp8_ctx4096"):
             if name == wl.name:
                 continue
             w2 = S.WORKLOADS[name]
             r2, _ = run_workload(w2, min(args.steps, w2.steps), args.warmup, mk, None, e2e_steps=16)
             variants[name] = {"tok_s": round(r2["tok_s"], 1), "ms_per_step": round(r2["ms_per_step"], 4),
+                              "watts": round(r2["watts"], 1) if r2["watts"] else None,
                               "weight_gbs": round(r2["weight_gbs"], 1),
                               "roofline_frac_weights": round(r2["weight_gbs"] / peak, 4),
                               "roofline_frac_weights_kv": round(r2["total_gbs"] / peak, 4),
                               "e2e_tok_s": round(r2["e2e_tok_s"], 1), "clocks": r2["clocks"]}
+    xr = None
+    if rank == 0 and not args.no_xray and not wl.prefill:
+        xr = xray_summary(wl, mk, master)
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = oracle_sample(wl, master, seconds=12.0)
@@ -397,6 +475,10 @@ def main():
                 "d2h_bytes_per_step": 256, "api": "mk_decode_step (token in with the launch, status+token back)"},
         "gpu_launches": args.steps,
         "clocks": res["clocks"],
+        "energy": {"watts": round(res["watts"], 1) if res["watts"] else None,
+                   "tok_per_joule": round(value / world / res["watts"], 2) if res["watts"] else None,
+                   "source": "NVML board power, median over the timed region"},
+        "xray": xr,
         "variants": variants,
     }
     print(json.dumps(line))

@@ -8,7 +8,7 @@ from tests.gpu_util import compare_step, make_pair
 pytestmark = pytest.mark.gpu
 
 
-@pytest.mark.parametrize("name", ["qwen3_0.6b_bf16", "qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4"])
+@pytest.mark.parametrize("name", ["qwen3_0.6b_bf16", "qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4", "qwen3_0.6b_fp8_bf16head"])
 def test_full_model_prompt_then_greedy(name):
     wl = S.WORKLOADS[name]
     cfg = wl.config()
