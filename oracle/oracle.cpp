@@ -284,6 +284,64 @@ void quant_fp8_row(const uint16_t* w, int rows, int cols, uint8_t* codes, float*
   });
 }
 
+// The E2M1 codes of one 16-element block for block-scale code `bc` (binary32 quotient, as in
+// quant_nvfp4) and the block's squared reconstruction error, summed in double in element order.
+double nvfp4_block(const uint16_t* p, uint8_t bc, float t, uint8_t* nib) {
+  volatile float bval = (float)e4m3_value(bc);
+  volatile float denom = bval * t;
+  double err = 0.0;
+  for (int j = 0; j < 16; ++j) {
+    nib[j] = 0;
+    if (denom != 0.0f) {
+      volatile float q = bf16_as_float(p[j]) / denom;
+      nib[j] = e2m1_encode((double)q);
+    }
+    const double rec = e2m1_value(nib[j]) * e4m3_value(bc) * (double)t;
+    const double d = bf16_value(p[j]) - rec;
+    err += d * d;
+  }
+  return err;
+}
+
+// NVFP4 with the per-block scale search the pages ask for ("round to nearest plus a per-block
+// scale search that minimizes MSE", monolith page, "Design decisions", NVFP4 format). Reading:
+// the tensor scale is the amax one of quant_nvfp4; every E4M3 code 0 .. 0x7E (all non-negative
+// finite block scales) is a candidate; a candidate's E2M1 codes are round-to-nearest as in
+// quant_nvfp4 and its error is the summed squared reconstruction error of the block; the least
+// error wins, ties to the smaller code (so an all-zero block keeps code 0).
+void quant_nvfp4_mse(const uint16_t* w, int rows, int cols, uint8_t* codes, uint8_t* bscales,
+                     float* tscale_out, int nthreads) {
+  float amax_t = 0.0f;
+  for (size_t i = 0; i < (size_t)rows * cols; ++i)
+    amax_t = std::max(amax_t, (float)std::fabs(bf16_value(w[i])));
+  volatile float t = amax_t / 2688.0f;
+  *tscale_out = t;
+  parallel_rows(rows, nthreads, [&](int r0, int r1) {
+  for (int r = r0; r < r1; ++r) {
+    for (int b = 0; b < cols / 16; ++b) {
+      const uint16_t* p = w + (size_t)r * cols + (size_t)b * 16;
+      uint8_t best = 0, nib[16], bnib[16];
+      double besterr = nvfp4_block(p, 0, t, bnib);
+      for (int c = 1; c <= 0x7E; ++c) {
+        const double e = nvfp4_block(p, (uint8_t)c, t, nib);
+        if (e < besterr) {
+          besterr = e;
+          best = (uint8_t)c;
+          std::memcpy(bnib, nib, 16);
+        }
+      }
+      bscales[(size_t)r * (cols / 16) + b] = best;
+      for (int j = 0; j < 16; ++j) {
+        size_t k = (size_t)b * 16 + j;
+        uint8_t& byte = codes[(size_t)r * (cols / 2) + k / 2];
+        if (k % 2 == 0) byte = (uint8_t)((byte & 0xF0) | bnib[j]);
+        else byte = (uint8_t)((byte & 0x0F) | (bnib[j] << 4));
+      }
+    }
+  }
+  });
+}
+
 void quant_nvfp4(const uint16_t* w, int rows, int cols, uint8_t* codes, uint8_t* bscales,
                  float* tscale_out, int nthreads) {
   float amax_t = 0.0f;
@@ -440,6 +498,10 @@ void or_quant_fp8_row(const uint16_t* w, int rows, int cols, uint8_t* codes, flo
 void or_quant_nvfp4(const uint16_t* w, int rows, int cols, uint8_t* codes, uint8_t* bscales,
                     float* tscale, int nthreads) {
   quant_nvfp4(w, rows, cols, codes, bscales, tscale, nthreads);
+}
+void or_quant_nvfp4_mse(const uint16_t* w, int rows, int cols, uint8_t* codes, uint8_t* bscales,
+                        float* tscale, int nthreads) {
+  quant_nvfp4_mse(w, rows, cols, codes, bscales, tscale, nthreads);
 }
 void or_attend(const double* q, const uint16_t* K, const uint16_t* V, int n, int d, double* out) {
   attend(q, K, V, n, d, out);

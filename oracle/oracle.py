@@ -116,14 +116,15 @@ def quant_fp8_row(w_bf16: np.ndarray, nthreads=None):
     return codes, scales
 
 
-def quant_nvfp4(w_bf16: np.ndarray, nthreads=None):
+def quant_nvfp4(w_bf16: np.ndarray, nthreads=None, scale_search=False):
     w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
     rows, cols = w.shape
     assert cols % 16 == 0
     codes = np.zeros((rows, cols // 2), np.uint8)
     bscales = np.zeros((rows, cols // 16), np.uint8)
     t = np.zeros(1, np.float32)
-    lib().or_quant_nvfp4(_p(w), rows, cols, _p(codes), _p(bscales), _p(t), _nt(nthreads))
+    fn = lib().or_quant_nvfp4_mse if scale_search else lib().or_quant_nvfp4
+    fn(_p(w), rows, cols, _p(codes), _p(bscales), _p(t), _nt(nthreads))
     return codes, bscales, float(t[0])
 
 
@@ -142,14 +143,17 @@ def pack(w_bf16: np.ndarray, fmt: int) -> PackedMat:
 def pack_model(master, fmap, nthreads=None):
     """Quantise every matrix of a bf16 master-weight dict with the oracle's own quantisers.
     master: {"embed", "layers": [{"q".."down", "ln_in", "ln_post", "q_norm", "k_norm"}], "final_norm"}
-    fmap: {"embed": fmt, "q": fmt, ...}."""
+    fmap: {"embed": fmt, "q": fmt, ...}; fmap["scale_search"] (optional) selects the NVFP4
+    block-scale search."""
+    search = bool(fmap.get("scale_search", False))
+
     def pk(w, fmt):
         if fmt == FMT_BF16:
             return PackedMat(fmt, w.shape[0], w.shape[1], w)
         if fmt == FMT_FP8_ROW:
             c, s = quant_fp8_row(w, nthreads)
             return PackedMat(fmt, w.shape[0], w.shape[1], c, s)
-        c, b, t = quant_nvfp4(w, nthreads)
+        c, b, t = quant_nvfp4(w, nthreads, search)
         return PackedMat(fmt, w.shape[0], w.shape[1], c, b, t)
 
     out = {"embed": pk(master["embed"], fmap["embed"]), "final_norm": master["final_norm"], "layers": []}

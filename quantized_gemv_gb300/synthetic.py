@@ -56,10 +56,12 @@ def format_map(variant: str):
     elif variant == "fp8_bf16head":  # FP8 layers, bf16 tied embedding / LM head
         m = {n: FMT_FP8_ROW for n in LINEARS}
         m["embed"] = FMT_BF16
-    elif variant == "nvfp4":
+    elif variant in ("nvfp4", "nvfp4_mse"):  # _mse: block scales chosen by least squared error
         m = {n: FMT_NVFP4 for n in ("q", "k", "v", "o", "gate", "up")}
         m["down"] = FMT_FP8_ROW
         m["embed"] = FMT_FP8_ROW
+        if variant == "nvfp4_mse":
+            m["scale_search"] = True
     else:
         raise ValueError(variant)
     return m
@@ -150,6 +152,9 @@ WORKLOADS = {
                                "28-layer FP8-E4M3 per-row incl. LM head, 32-token prompt, 256 greedy steps"),
     "qwen3_0.6b_nvfp4": Workload("qwen3_0.6b_nvfp4", "nvfp4", 28, 32, 0, 256,
                                  "NVFP4 q/k/v/o/gate/up, FP8 down + LM head, 32-token prompt, 256 greedy steps"),
+    "qwen3_0.6b_nvfp4_mse": Workload("qwen3_0.6b_nvfp4_mse", "nvfp4_mse", 28, 32, 0, 256,
+                                     "NVFP4 as qwen3_0.6b_nvfp4 with least-squared-error block scales, "
+                                     "32-token prompt, 256 greedy steps"),
     "qwen3_0.6b_fp8_bf16head": Workload("qwen3_0.6b_fp8_bf16head", "fp8_bf16head", 28, 32, 0, 256,
                                         "28-layer FP8-E4M3 per-row, bf16 tied embedding and LM head, 32-token "
                                         "prompt, 256 greedy steps"),

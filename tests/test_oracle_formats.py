@@ -130,6 +130,81 @@ def test_quant_fp8_error_bound_and_zero_row():
     assert np.all(np.abs(deq).max(axis=1)[np.arange(40) != 3] <= scales[np.arange(40) != 3] * 448 * (1 + 1e-6))
 
 
+
+def _e2m1_round(q, grid):
+    """Vectorised brute force: nearest printed E2M1 magnitude (ties to the even code, saturating
+    at 6); returns the codes with the sign bit of q."""
+    g = np.asarray(grid)
+    a = np.abs(q)
+    d = np.abs(a[..., None] - g)
+    hit = d == d.min(-1, keepdims=True)
+    even = np.where(hit & (np.arange(8) % 2 == 0), np.arange(8), 99).min(-1)
+    k = np.where(even < 99, even, np.where(hit, np.arange(8), 99).min(-1))
+    k = np.where(a >= 6, 7, k)
+    return k | np.where(np.signbit(q), 8, 0)
+
+
+def test_quant_nvfp4_scale_search_bruteforce():
+    """Every block scale tried by brute force (torch float8 decode, fp32 torch division, the
+    printed grid): the oracle's choice has the least squared error, no smaller code reaches it,
+    and its E2M1 codes are the round-to-nearest ones for that scale."""
+    grid = golden_e2m1_grid()
+    rows, cols = 24, 160
+    w = S.random_matrix(rows, cols, seed=17)
+    w[5, 32:48] = 0                                                  # an all-zero block
+    w[6, 0:16] = S.random_matrix(1, 16, seed=18, std=1e-5)[0]        # a block far below the tensor amax
+    codes, bscales, t = O.quant_nvfp4(w, scale_search=True)
+    wf32 = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).to(torch.float32)
+    assert t == float(wf32.abs().max() / torch.tensor(2688.0))
+    blocks = wf32.view(rows, cols // 16, 16)
+    e4 = torch.arange(127, dtype=torch.uint8).view(torch.float8_e4m3fn).to(torch.float32)
+    denom = e4 * torch.tensor(t, dtype=torch.float32)                        # fp32, one per code
+    q = (blocks[:, :, None, :] / denom[None, None, :, None]).numpy()        # [r][b][code][j]
+    nib = _e2m1_round(np.nan_to_num(q, nan=0.0, posinf=0.0, neginf=0.0), grid)
+    nib[:, :, denom.numpy() == 0, :] = 0
+    val = np.asarray(grid)[nib & 7] * np.where(nib & 8, -1.0, 1.0)
+    rec = val * e4.double().numpy()[None, None, :, None] * float(t)
+    err = ((blocks.double().numpy()[:, :, None, :] - rec) ** 2).sum(-1)    # [r][b][code]
+    for r in range(rows):
+        for b in range(cols // 16):
+            c = int(bscales[r, b])
+            e = err[r, b]
+            assert e[c] <= e.min() * (1 + 1e-12), (r, b, c, int(e.argmin()))
+            assert np.all(e[:c] > e[c] * (1 + 1e-12)), (r, b, c)
+            got = [(codes[r, (16 * b + j) // 2] >> (4 * (j % 2))) & 0xF for j in range(16)]
+            assert got == list(nib[r, b, c]), (r, b)
+    assert not bscales[5, 2] and not codes[5, 16:24].any()
+    # never worse than the amax block scale, block by block, and better overall
+    ca, ba, ta = O.quant_nvfp4(w)
+    sse_s = err[np.arange(rows)[:, None], np.arange(cols // 16)[None, :], bscales]
+    deq_a = O.dequant(O.PackedMat(O.FMT_NVFP4, rows, cols, ca, ba, ta)).reshape(rows, cols // 16, 16)
+    sse_a = ((deq_a - blocks.double().numpy()) ** 2).sum(-1)
+    assert np.all(sse_s <= sse_a * (1 + 1e-12))
+    assert sse_s.sum() < 0.9 * sse_a.sum()
+
+
+def test_quant_nvfp4_scale_search_worked_ties():
+    """Hand-worked blocks at tensor scale t = 1 (tensor amax 2688 = 6 * 448):
+    - {2688}: code 0x7E (448) puts it exactly on 6; no other scale is exact, since 2688/4 > 448.
+    - {-10, -12}: scale 3 (code 68) gives -9, -12 and scale 6 (code 76) gives -9, -12 as well;
+      both have squared error 1, the least of all scales; the tie goes to the smaller code, 68.
+    - {-1, 5}: scale 0.8125 (code 53) gives -0.8125 and 4.875 (5/0.8125 saturates at 6), scale
+      1.625 (code 61) gives -0.8125 and 4.875 (5/1.625 rounds to 3); error 0.05078125 each; 53.
+    - all zero: code 0."""
+    def bits(x):
+        return int(torch.tensor(x, dtype=torch.bfloat16).view(torch.int16)) & 0xFFFF
+    w = np.zeros((4, 16), np.uint16)
+    w[0, 0] = bits(2688.0)
+    w[1, 3], w[1, 9] = bits(-10.0), bits(-12.0)
+    w[2, 7], w[2, 3] = bits(-1.0), bits(5.0)
+    codes, bscales, t = O.quant_nvfp4(w, scale_search=True)
+    assert t == 1.0
+    assert list(bscales[:, 0]) == [0x7E, 68, 53, 0]
+    deq = O.dequant(O.PackedMat(O.FMT_NVFP4, 4, 16, codes, bscales, t))
+    assert deq[0, 0] == 2688.0 and deq[1, 3] == -9.0 and deq[1, 9] == -12.0
+    assert deq[2, 7] == -0.8125 and deq[2, 3] == 4.875
+    assert not deq[3].any() and np.count_nonzero(deq) == 5
+
 def test_quant_nvfp4_bruteforce():
     grid = golden_e2m1_grid()
     table = {c: grid[c] for c in range(8)}
