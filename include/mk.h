@@ -162,6 +162,17 @@ int mk_pack_fp8_row(const void* w_bf16_dev, int rows, int cols, void* codes_dev,
 int mk_pack_nvfp4(const void* w_bf16_dev, int rows, int cols, void* codes_dev, void* bscales_dev,
                   float* tscale_dev, void* stream);
 
+/* MK_NVFP4 with a per-block scale search (the monolith page, "Design decisions", NVFP4 format:
+ * round to nearest plus a block-scale choice that minimises the squared error). t as in
+ * mk_pack_nvfp4. Every E4M3 code b in 0 .. 0x7E is tried for each block: its codes are formed
+ * with the mk_pack_nvfp4 quotient rule (all zero when fp32(e4m3(b) * t) is 0) and its error is
+ * sum_j (w_j - e2m1(code_j) * e4m3(b) * t)^2 in double, in element order, without fused
+ * multiply-add; the least error wins, ties to the smaller b (an all-zero block keeps b = 0).
+ * Same arguments, layouts and errors as mk_pack_nvfp4 (MK_EINVAL for NULL pointers or cols not
+ * a positive multiple of 16). */
+int mk_pack_nvfp4_mse(const void* w_bf16_dev, int rows, int cols, void* codes_dev, void* bscales_dev,
+                      float* tscale_dev, void* stream);
+
 /* y = W x with the same streaming dequant-GEMV the megakernel uses, as one persistent launch.
  * x_dev: fp32 [cols]; y_dev: fp32 [rows]; cols a multiple of 1024 and at most 4096. */
 int mk_gemv(const mk_mat* w, int rows, int cols, const float* x_dev, float* y_dev, void* stream);

@@ -417,6 +417,11 @@ int mk_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales,
   return launch_pack_nvfp4(w, rows, cols, codes, bscales, tscale, stream) ? MK_ECUDA : MK_OK;
 }
 
+int mk_pack_nvfp4_mse(const void* w, int rows, int cols, void* codes, void* bscales, float* tscale, void* stream) {
+  if (!w || !codes || !bscales || !tscale || rows < 1 || cols < 16 || cols % 16) return MK_EINVAL;
+  return launch_pack_nvfp4_mse(w, rows, cols, codes, bscales, tscale, stream) ? MK_ECUDA : MK_OK;
+}
+
 int mk_gemv(const mk_mat* w, int rows, int cols, const float* x, float* y, void* stream) {
   if (!w || !x || !y || rows < 1 || cols < 1024 || cols % 1024 || cols > XS_MAX) return MK_EINVAL;
   if (w->fmt < 0 || w->fmt > 2 || !w->data || !aligned16(w->data)) return MK_EINVAL;

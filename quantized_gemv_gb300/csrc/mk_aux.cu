@@ -89,6 +89,64 @@ __global__ void k_pack_nvfp4(const uint16_t* __restrict__ w, int rows, int cols,
   }
 }
 
+// The value of an E2M1 code (hardware decode of the low nibble).
+__device__ __forceinline__ double e2m1_to_d(uint32_t nib) {
+  uint32_t h;
+  asm("{ .reg .b8 t; cvt.u8.u32 t, %1; cvt.rn.f16x2.e2m1x2 %0, t; }" : "=r"(h) : "r"(nib & 0xFu));
+  return (double)__half2float(__ushort_as_half((uint16_t)(h & 0xFFFFu)));
+}
+
+// Codes of one 16-element block for block-scale code c (same quotient rule as k_pack_nvfp4) and its
+// squared reconstruction error, summed in double in element order with no fused multiply-add.
+__device__ double nvfp4_block_err(const float* v, uint32_t c, float t, uint8_t* out) {
+  const float ef = e4m3_to_f((uint8_t)c);
+  const float denom = __fmul_rn(ef, t);
+  const double sc = __dmul_rn((double)ef, (double)t);
+  double err = 0.0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t byte = 0;
+    if (denom != 0.f) byte = f32x2_to_e2m1x2(__fdiv_rn(v[2 * j], denom), __fdiv_rn(v[2 * j + 1], denom));
+    out[j] = (uint8_t)byte;
+    const double d0 = __dsub_rn((double)v[2 * j], __dmul_rn(e2m1_to_d(byte), sc));
+    err = __dadd_rn(err, __dmul_rn(d0, d0));
+    const double d1 = __dsub_rn((double)v[2 * j + 1], __dmul_rn(e2m1_to_d(byte >> 4), sc));
+    err = __dadd_rn(err, __dmul_rn(d1, d1));
+  }
+  return err;
+}
+
+// NVFP4 with a per-block scale search: one thread per 16-element block tries every E4M3 code
+// 0 .. 0x7E as its block scale and keeps the one with the least squared reconstruction error,
+// ties to the smaller code (an all-zero block keeps code 0).
+__global__ void k_pack_nvfp4_mse(const uint16_t* __restrict__ w, int rows, int cols, uint8_t* __restrict__ codes,
+                                 uint8_t* __restrict__ bscales, const float* __restrict__ tscale) {
+  const size_t nb = (size_t)rows * (cols / 16);
+  const size_t blk = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (blk >= nb) return;
+  const float t = tscale[0];
+  const uint16_t* src = w + blk * 16;
+  float v[16];
+#pragma unroll
+  for (int j = 0; j < 16; ++j) v[j] = bf16_to_f(src[j]);
+  uint8_t best[8], cand[8];
+  uint32_t bc = 0;
+  double be = nvfp4_block_err(v, 0, t, best);
+  for (uint32_t c = 1; c <= 0x7Eu; ++c) {
+    const double e = nvfp4_block_err(v, c, t, cand);
+    if (e < be) {
+      be = e;
+      bc = c;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) best[j] = cand[j];
+    }
+  }
+  bscales[blk] = (uint8_t)bc;
+  uint8_t* out = codes + blk * 8;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) out[j] = best[j];
+}
+
 // ---------------------------------------------------------------- RoPE table
 // cos/sin of pos * theta^(-2i/128), angle and trig in double, stored as fp32.
 __global__ void k_rope_table(float* cosb, float* sinb, int max_ctx, double theta) {
@@ -142,6 +200,20 @@ int launch_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bsca
   const size_t nb = (size_t)rows * (cols / 16);
   k_pack_nvfp4<<<(unsigned)((nb + 255) / 256), 256, 0, st>>>((const uint16_t*)w, rows, cols, (uint8_t*)codes,
                                                                (uint8_t*)bscales, t);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
+int launch_pack_nvfp4_mse(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream) {
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaMemsetAsync(t, 0, sizeof(float), st) != cudaSuccess) return -1;
+  const size_t n = (size_t)rows * cols;
+  int blocks = (int)((n + 255) / 256);
+  if (blocks > 4096) blocks = 4096;
+  k_amax<<<blocks, 256, 0, st>>>((const uint16_t*)w, n, (uint32_t*)t);
+  k_tscale<<<1, 1, 0, st>>>(t);
+  const size_t nb = (size_t)rows * (cols / 16);
+  k_pack_nvfp4_mse<<<(unsigned)((nb + 127) / 128), 128, 0, st>>>((const uint16_t*)w, rows, cols, (uint8_t*)codes,
+                                                                   (uint8_t*)bscales, t);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -122,6 +122,7 @@ int launch_stream_read(const void* buf, size_t bytes, int grid, void* stream);
 int launch_rope_table(float* cosb, float* sinb, int max_ctx, float theta, void* stream);
 int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, void* stream);
 int launch_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
+int launch_pack_nvfp4_mse(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
 int launch_probe_cvt(uint32_t* a, uint32_t* b, const float* in, int n, uint16_t* e4, uint8_t* e2, void* stream);
 int decode_occupancy(int* blocks_per_sm);
 // Record an error text for mk_last_error(NULL) (mk_api.cu).

@@ -53,7 +53,7 @@ class mk_weights(C.Structure):
 # every symbol include/mk.h declares
 EXPORTS = ("mk_max_context", "mk_decode_grid", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
            "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
-           "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
+           "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_pack_nvfp4_mse", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
            "mk_decode_step_static")
 
 _lib = None
@@ -83,6 +83,7 @@ def lib():
         L.mk_debug_fault.argtypes = [vp, C.c_int, C.c_int, C.c_int]
         L.mk_pack_fp8_row.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp]
         L.mk_pack_nvfp4.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
+        L.mk_pack_nvfp4_mse.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
         L.mk_gemv.argtypes = [C.POINTER(mk_mat), C.c_int, C.c_int, vp, vp, vp]
         L.mk_stream_read.argtypes = [vp, sz, vp]
         L.mk_probe_cvt.argtypes = [vp, vp, vp, C.c_int, vp, vp, vp]
@@ -136,26 +137,29 @@ def pack_fp8_row(w_bf16: torch.Tensor, stream=None):
     return codes, scales
 
 
-def pack_nvfp4(w_bf16: torch.Tensor, stream=None):
+def pack_nvfp4(w_bf16: torch.Tensor, stream=None, scale_search=False):
+    """NVFP4 codes, E4M3 block scales and the fp32 tensor scale (a device scalar). With
+    scale_search, each block's scale is the least-squared-error one (mk_pack_nvfp4_mse)."""
     _need_cuda(w_bf16)
     rows, cols = w_bf16.shape
     dev = w_bf16.device
     codes = torch.empty((rows, cols // 2), dtype=torch.uint8, device=dev)
     bscales = torch.empty((rows, cols // 16), dtype=torch.uint8, device=dev)
     t = torch.empty(1, dtype=torch.float32, device=dev)
-    _check(lib().mk_pack_nvfp4(_ptr(w_bf16.contiguous()), rows, cols, _ptr(codes), _ptr(bscales), _ptr(t),
-                               _stream(stream)), what="mk_pack_nvfp4")
+    fn, name = (lib().mk_pack_nvfp4_mse, "mk_pack_nvfp4_mse") if scale_search else (lib().mk_pack_nvfp4,
+                                                                                      "mk_pack_nvfp4")
+    _check(fn(_ptr(w_bf16.contiguous()), rows, cols, _ptr(codes), _ptr(bscales), _ptr(t), _stream(stream)), what=name)
     return codes, bscales, t
 
 
-def pack(w_bf16: torch.Tensor, fmt: int, stream=None) -> PackedMat:
+def pack(w_bf16: torch.Tensor, fmt: int, stream=None, scale_search=False) -> PackedMat:
     rows, cols = w_bf16.shape
     if fmt == FMT_BF16:
         return PackedMat(fmt, rows, cols, w_bf16.contiguous())
     if fmt == FMT_FP8_ROW:
         c, s = pack_fp8_row(w_bf16, stream)
         return PackedMat(fmt, rows, cols, c, s)
-    c, b, t = pack_nvfp4(w_bf16, stream)
+    c, b, t = pack_nvfp4(w_bf16, stream, scale_search)
     torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
     return PackedMat(fmt, rows, cols, c, b, float(t.item()))
 
@@ -317,9 +321,12 @@ def upload_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
 
 
 def pack_model(master, fmap, device="cuda"):
-    """Upload bf16 master weights and quantise them on the device with the library's packers."""
+    """Upload bf16 master weights and quantise them on the device with the library's packers.
+    fmap["scale_search"] (optional) selects the NVFP4 block-scale search."""
+    search = bool(fmap.get("scale_search", False))
+
     def pk(bits, fmt):
-        return pack(upload_bf16(bits, device), fmt)
+        return pack(upload_bf16(bits, device), fmt, scale_search=search)
 
     out = {"embed": pk(master["embed"], fmap["embed"]), "final_norm": upload_bf16(master["final_norm"], device),
            "layers": []}

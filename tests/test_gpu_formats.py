@@ -72,6 +72,19 @@ def test_pack_nvfp4_bit_exact(shape):
     assert np.array_equal(codes.cpu().numpy(), oc)
 
 
+
+@pytest.mark.parametrize("shape", [(9, 96), (33, 1024), (3072, 1024)])
+def test_pack_nvfp4_scale_search_bit_exact(shape):
+    """The block-scale search packer against the oracle's, up to a full-size gate matrix."""
+    w = S.random_matrix(*shape, seed=24)
+    w[0, 16:32] = 0
+    w[-1, -16:] = S.random_matrix(1, 16, seed=25, std=1e-5)[0]
+    codes, bs, t = mk.pack_nvfp4(mk.upload_bf16(w), scale_search=True)
+    oc, ob, ot = O.quant_nvfp4(w, scale_search=True)
+    assert np.float32(t.item()).view(np.uint32) == np.float32(ot).view(np.uint32)
+    assert np.array_equal(bs.cpu().numpy(), ob)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
 def test_pack_full_size_lm_head_bit_exact():
     """The full 151,936 x 1024 tied matrix, FP8 per row, as the benchmark packs it."""
     w = S.random_matrix(151936, 1024, seed=23)
