@@ -14,8 +14,8 @@ Extra keys beyond the base contract: `roofline` (the decode kernel against the m
 bandwidth), `cpu_baseline` (the CPU oracle on this host's cores, a bounded sample), `e2e` (the
 same metric through mk_decode_step, which returns each token to the host), `clocks` (NVML samples
 during the timed region), `stream_read_gbs` (the library's bulk-copy streaming-read probe, same
-run) and `variants` (the FP8, NVFP4 (amax and searched block scales), bf16-head FP8 and long-context
-FP8 workloads, each timed the same way).
+run) and `variants` (the FP8, NVFP4 (amax and searched block scales; all-NVFP4), bf16-head FP8,
+bf16-scale FP8 and long-context FP8 workloads, each timed the same way).
 
 --impl reference times the CPU oracle (the only reference implementation of this method) on the
 same workload and prints its line with "impl": "reference". Under torchrun, rank 0 alone runs it.
@@ -433,8 +433,8 @@ def main():
     achieved = (res["weight_bytes"] + res["kv_bytes"]) / (res["launch_ms"] * 1e-3) / 1e9
     variants = {}
     if not args.no_variants and rank == 0:
-        for name in ("qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4", "qwen3_0.6b_nvfp4_mse", "qwen3_0.6b_fp8_bf16head",
-                     "qwen3_0.6b_fp8_ctx4096"):
+        for name in ("qwen3_0.6b_fp8", "qwen3_0.6b_nvfp4", "qwen3_0.6b_nvfp4_mse", "qwen3_0.6b_nvfp4_all",
+                     "qwen3_0.6b_fp8_bf16head", "qwen3_0.6b_fp8_bf16scale", "qwen3_0.6b_fp8_ctx4096"):
             if name == wl.name:
                 continue
             w2 = S.WORKLOADS[name]

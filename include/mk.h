@@ -155,6 +155,14 @@ int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms);
  * scale 0 and zero codes. codes_dev: [rows][cols] bytes; scales_dev: fp32 [rows]. */
 int mk_pack_fp8_row(const void* w_bf16_dev, int rows, int cols, void* codes_dev, float* scales_dev, void* stream);
 
+/* MK_FP8_ROW with bf16 row scales (the monolith page, "Design decisions", FP8 format, allows an
+ * fp32 or a bf16 scale): scale[r] = bf16_RNE(fp32(absmax/448)), stored widened in the same fp32
+ * array (its low 16 bits are zero), code = E4M3 round-to-nearest-even, saturating, of
+ * fp32(w / scale[r]); a row whose scale rounded down may saturate its maximum at 448. Same
+ * arguments, layouts and errors as mk_pack_fp8_row. */
+int mk_pack_fp8_row_bf16scale(const void* w_bf16_dev, int rows, int cols, void* codes_dev, float* scales_dev,
+                              void* stream);
+
 /* Quantise a bf16 matrix into MK_NVFP4 on the device (cols a multiple of 16):
  * t = fp32(amax/2688); block scale b = E4M3_RNE(fp32(amax_block / fp32(6 t))); code =
  * E2M1_RNE_satfinite(fp32(w / fp32(e4m3(b) * t))). tscale_dev (device fp32) receives t; it is

@@ -263,14 +263,18 @@ int argmax_lowest(const double* x, int n) {
 //          b = E4M3_RNE_satfinite(fp32(amax_block / fp32(6 * t)))
 //          code = E2M1_RNE_satfinite(fp32(w / fp32(value(b) * t)))
 // A zero scale (all-zero row, block or tensor) gives all-zero codes.
+// bf16_scale: the row scale is a bf16 number (the monolith page, "Design decisions", FP8 format,
+// allows an fp32 or a bf16 scale): fp32(absmax / 448) rounded to nearest-even bf16; the elements
+// are then divided by that scale, so the row maximum may saturate at 448.
 void quant_fp8_row(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales,
-                   int nthreads) {
+                   int nthreads, bool bf16_scale = false) {
   parallel_rows(rows, nthreads, [&](int r0, int r1) {
   for (int r = r0; r < r1; ++r) {
     const uint16_t* p = w + (size_t)r * cols;
     float amax = 0.0f;
     for (int k = 0; k < cols; ++k) amax = std::max(amax, (float)std::fabs(bf16_value(p[k])));
     volatile float s = amax / 448.0f;
+    if (bf16_scale) s = (float)bf16_value(bf16_encode((double)s));
     scales[r] = s;
     for (int k = 0; k < cols; ++k) {
       if (s == 0.0f) {
@@ -494,6 +498,10 @@ int or_bf16_encode(double v) { return bf16_encode(v); }
 void or_quant_fp8_row(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales,
                       int nthreads) {
   quant_fp8_row(w, rows, cols, codes, scales, nthreads);
+}
+void or_quant_fp8_row_bf16scale(const uint16_t* w, int rows, int cols, uint8_t* codes, float* scales,
+                                int nthreads) {
+  quant_fp8_row(w, rows, cols, codes, scales, nthreads, true);
 }
 void or_quant_nvfp4(const uint16_t* w, int rows, int cols, uint8_t* codes, uint8_t* bscales,
                     float* tscale, int nthreads) {

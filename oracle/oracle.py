@@ -107,12 +107,13 @@ def _nt(n):
     return len(os.sched_getaffinity(0)) if n is None else int(n)
 
 
-def quant_fp8_row(w_bf16: np.ndarray, nthreads=None):
+def quant_fp8_row(w_bf16: np.ndarray, nthreads=None, bf16_scale=False):
     w = np.ascontiguousarray(w_bf16, dtype=np.uint16)
     rows, cols = w.shape
     codes = np.zeros((rows, cols), np.uint8)
     scales = np.zeros(rows, np.float32)
-    lib().or_quant_fp8_row(_p(w), rows, cols, _p(codes), _p(scales), _nt(nthreads))
+    fn = lib().or_quant_fp8_row_bf16scale if bf16_scale else lib().or_quant_fp8_row
+    fn(_p(w), rows, cols, _p(codes), _p(scales), _nt(nthreads))
     return codes, scales
 
 
@@ -144,14 +145,15 @@ def pack_model(master, fmap, nthreads=None):
     """Quantise every matrix of a bf16 master-weight dict with the oracle's own quantisers.
     master: {"embed", "layers": [{"q".."down", "ln_in", "ln_post", "q_norm", "k_norm"}], "final_norm"}
     fmap: {"embed": fmt, "q": fmt, ...}; fmap["scale_search"] (optional) selects the NVFP4
-    block-scale search."""
+    block-scale search, fmap["bf16_scale"] (optional) bf16 FP8 row scales."""
     search = bool(fmap.get("scale_search", False))
+    bf16s = bool(fmap.get("bf16_scale", False))
 
     def pk(w, fmt):
         if fmt == FMT_BF16:
             return PackedMat(fmt, w.shape[0], w.shape[1], w)
         if fmt == FMT_FP8_ROW:
-            c, s = quant_fp8_row(w, nthreads)
+            c, s = quant_fp8_row(w, nthreads, bf16s)
             return PackedMat(fmt, w.shape[0], w.shape[1], c, s)
         c, b, t = quant_nvfp4(w, nthreads, search)
         return PackedMat(fmt, w.shape[0], w.shape[1], c, b, t)

@@ -409,7 +409,12 @@ int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms) {
 
 int mk_pack_fp8_row(const void* w, int rows, int cols, void* codes, float* scales, void* stream) {
   if (!w || !codes || !scales || rows < 1 || cols < 2 || cols % 2) return MK_EINVAL;
-  return launch_pack_fp8(w, rows, cols, codes, scales, stream) ? MK_ECUDA : MK_OK;
+  return launch_pack_fp8(w, rows, cols, codes, scales, 0, stream) ? MK_ECUDA : MK_OK;
+}
+
+int mk_pack_fp8_row_bf16scale(const void* w, int rows, int cols, void* codes, float* scales, void* stream) {
+  if (!w || !codes || !scales || rows < 1 || cols < 2 || cols % 2) return MK_EINVAL;
+  return launch_pack_fp8(w, rows, cols, codes, scales, 1, stream) ? MK_ECUDA : MK_OK;
 }
 
 int mk_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales, float* tscale, void* stream) {

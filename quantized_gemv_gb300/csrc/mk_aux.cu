@@ -28,9 +28,10 @@ __device__ __forceinline__ float e4m3_to_f(uint8_t c) {
 }
 
 // ---------------------------------------------------------------- FP8 per-row packer
-// One warp per row: scale = fp32(absmax / 448); code = E4M3_RNE_satfinite(fp32(w / scale)).
+// One warp per row: scale = fp32(absmax / 448), rounded to nearest-even bf16 when bf16_scale;
+// code = E4M3_RNE_satfinite(fp32(w / scale)).
 __global__ void k_pack_fp8(const uint16_t* __restrict__ w, int rows, int cols, uint8_t* __restrict__ codes,
-                           float* __restrict__ scales) {
+                           float* __restrict__ scales, int bf16_scale) {
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
   if (warp >= rows) return;
   const uint16_t* row = w + (size_t)warp * cols;
@@ -38,7 +39,11 @@ __global__ void k_pack_fp8(const uint16_t* __restrict__ w, int rows, int cols, u
   for (int k = lane; k < cols; k += 32) amax = fmaxf(amax, fabsf(bf16_to_f(row[k])));
 #pragma unroll
   for (int o = 16; o; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  const float s = __fdiv_rn(amax, 448.0f);
+  float s = __fdiv_rn(amax, 448.0f);
+  if (bf16_scale) {  // s is finite and non-negative: round the low 16 bits away, ties to even
+    const uint32_t u = __float_as_uint(s);
+    s = __uint_as_float((u + 0x7FFFu + ((u >> 16) & 1u)) & 0xFFFF0000u);
+  }
   if (lane == 0) scales[warp] = s;
   uint8_t* out = codes + (size_t)warp * cols;
   for (int k = 2 * lane; k < cols; k += 64) {
@@ -182,10 +187,11 @@ __global__ void k_probe_cvt(uint32_t* f16_e4m3, uint32_t* f16_e2m1, const float*
 }
 
 // ---------------------------------------------------------------- launchers
-int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, void* stream) {
+int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, int bf16_scale, void* stream) {
   const int threads = 256, warps_per_block = threads / 32;
   const int blocks = (rows + warps_per_block - 1) / warps_per_block;
-  k_pack_fp8<<<blocks, threads, 0, (cudaStream_t)stream>>>((const uint16_t*)w, rows, cols, (uint8_t*)codes, scales);
+  k_pack_fp8<<<blocks, threads, 0, (cudaStream_t)stream>>>((const uint16_t*)w, rows, cols, (uint8_t*)codes, scales,
+                                                           bf16_scale);
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 

@@ -120,7 +120,7 @@ int decode_smem_bytes();
 int launch_gemv(const DMat& m, int rows, int cols, const float* x, float* y, int grid, void* stream);
 int launch_stream_read(const void* buf, size_t bytes, int grid, void* stream);
 int launch_rope_table(float* cosb, float* sinb, int max_ctx, float theta, void* stream);
-int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, void* stream);
+int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, int bf16_scale, void* stream);
 int launch_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
 int launch_pack_nvfp4_mse(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
 int launch_probe_cvt(uint32_t* a, uint32_t* b, const float* in, int n, uint16_t* e4, uint8_t* e2, void* stream);

@@ -53,7 +53,7 @@ class mk_weights(C.Structure):
 # every symbol include/mk.h declares
 EXPORTS = ("mk_max_context", "mk_decode_grid", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
            "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
-           "mk_pack_fp8_row", "mk_pack_nvfp4", "mk_pack_nvfp4_mse", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
+           "mk_pack_fp8_row", "mk_pack_fp8_row_bf16scale", "mk_pack_nvfp4", "mk_pack_nvfp4_mse", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
            "mk_decode_step_static")
 
 _lib = None
@@ -82,6 +82,7 @@ def lib():
         L.mk_trace_dump.argtypes = [vp, vp, sz, C.POINTER(sz)]
         L.mk_debug_fault.argtypes = [vp, C.c_int, C.c_int, C.c_int]
         L.mk_pack_fp8_row.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp]
+        L.mk_pack_fp8_row_bf16scale.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp]
         L.mk_pack_nvfp4.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
         L.mk_pack_nvfp4_mse.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
         L.mk_gemv.argtypes = [C.POINTER(mk_mat), C.c_int, C.c_int, vp, vp, vp]
@@ -127,13 +128,16 @@ class PackedMat:
                       self.tensor_scale, self.fmt)
 
 
-def pack_fp8_row(w_bf16: torch.Tensor, stream=None):
+def pack_fp8_row(w_bf16: torch.Tensor, stream=None, bf16_scale=False):
+    """FP8-E4M3 codes and fp32 row scales; bf16_scale rounds each scale to bf16 first
+    (mk_pack_fp8_row_bf16scale)."""
     _need_cuda(w_bf16)
     rows, cols = w_bf16.shape
     codes = torch.empty((rows, cols), dtype=torch.uint8, device=w_bf16.device)
     scales = torch.empty(rows, dtype=torch.float32, device=w_bf16.device)
-    _check(lib().mk_pack_fp8_row(_ptr(w_bf16.contiguous()), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)),
-           what="mk_pack_fp8_row")
+    fn, name = (lib().mk_pack_fp8_row_bf16scale, "mk_pack_fp8_row_bf16scale") if bf16_scale else \
+        (lib().mk_pack_fp8_row, "mk_pack_fp8_row")
+    _check(fn(_ptr(w_bf16.contiguous()), rows, cols, _ptr(codes), _ptr(scales), _stream(stream)), what=name)
     return codes, scales
 
 
@@ -152,12 +156,12 @@ def pack_nvfp4(w_bf16: torch.Tensor, stream=None, scale_search=False):
     return codes, bscales, t
 
 
-def pack(w_bf16: torch.Tensor, fmt: int, stream=None, scale_search=False) -> PackedMat:
+def pack(w_bf16: torch.Tensor, fmt: int, stream=None, scale_search=False, bf16_scale=False) -> PackedMat:
     rows, cols = w_bf16.shape
     if fmt == FMT_BF16:
         return PackedMat(fmt, rows, cols, w_bf16.contiguous())
     if fmt == FMT_FP8_ROW:
-        c, s = pack_fp8_row(w_bf16, stream)
+        c, s = pack_fp8_row(w_bf16, stream, bf16_scale)
         return PackedMat(fmt, rows, cols, c, s)
     c, b, t = pack_nvfp4(w_bf16, stream, scale_search)
     torch.cuda.current_stream().synchronize() if stream is None else stream.synchronize()
@@ -322,11 +326,13 @@ def upload_bf16(bits: np.ndarray, device="cuda") -> torch.Tensor:
 
 def pack_model(master, fmap, device="cuda"):
     """Upload bf16 master weights and quantise them on the device with the library's packers.
-    fmap["scale_search"] (optional) selects the NVFP4 block-scale search."""
+    fmap["scale_search"] (optional) selects the NVFP4 block-scale search, fmap["bf16_scale"]
+    (optional) bf16 FP8 row scales."""
     search = bool(fmap.get("scale_search", False))
+    bf16s = bool(fmap.get("bf16_scale", False))
 
     def pk(bits, fmt):
-        return pack(upload_bf16(bits, device), fmt, scale_search=search)
+        return pack(upload_bf16(bits, device), fmt, scale_search=search, bf16_scale=bf16s)
 
     out = {"embed": pk(master["embed"], fmap["embed"]), "final_norm": upload_bf16(master["final_norm"], device),
            "layers": []}

@@ -53,6 +53,10 @@ def format_map(variant: str):
     elif variant == "fp8":
         m = {n: FMT_FP8_ROW for n in LINEARS}
         m["embed"] = FMT_FP8_ROW
+    elif variant == "fp8_bf16scale":  # FP8 everywhere, row scales rounded to bf16
+        m = {n: FMT_FP8_ROW for n in LINEARS}
+        m["embed"] = FMT_FP8_ROW
+        m["bf16_scale"] = True
     elif variant == "fp8_bf16head":  # FP8 layers, bf16 tied embedding / LM head
         m = {n: FMT_FP8_ROW for n in LINEARS}
         m["embed"] = FMT_BF16
@@ -62,6 +66,10 @@ def format_map(variant: str):
         m["embed"] = FMT_FP8_ROW
         if variant == "nvfp4_mse":
             m["scale_search"] = True
+    elif variant == "nvfp4_all":  # every linear NVFP4 (searched block scales), FP8 tied embedding / head
+        m = {n: FMT_NVFP4 for n in LINEARS}
+        m["embed"] = FMT_FP8_ROW
+        m["scale_search"] = True
     else:
         raise ValueError(variant)
     return m
@@ -155,6 +163,12 @@ WORKLOADS = {
     "qwen3_0.6b_nvfp4_mse": Workload("qwen3_0.6b_nvfp4_mse", "nvfp4_mse", 28, 32, 0, 256,
                                      "NVFP4 as qwen3_0.6b_nvfp4 with least-squared-error block scales, "
                                      "32-token prompt, 256 greedy steps"),
+    "qwen3_0.6b_nvfp4_all": Workload("qwen3_0.6b_nvfp4_all", "nvfp4_all", 28, 32, 0, 256,
+                                     "every linear NVFP4 incl. down (least-squared-error block scales), FP8 LM "
+                                     "head, 32-token prompt, 256 greedy steps"),
+    "qwen3_0.6b_fp8_bf16scale": Workload("qwen3_0.6b_fp8_bf16scale", "fp8_bf16scale", 28, 32, 0, 256,
+                                         "28-layer FP8-E4M3 incl. LM head, bf16 row scales, 32-token prompt, "
+                                         "256 greedy steps"),
     "qwen3_0.6b_fp8_bf16head": Workload("qwen3_0.6b_fp8_bf16head", "fp8_bf16head", 28, 32, 0, 256,
                                         "28-layer FP8-E4M3 per-row, bf16 tied embedding and LM head, 32-token "
                                         "prompt, 256 greedy steps"),

@@ -12,7 +12,7 @@ pytestmark = pytest.mark.gpu
 SMALL = S.ModelConfig(n_layers=2, vocab=4099, max_ctx=1024)
 
 
-@pytest.mark.parametrize("variant", ["bf16", "fp8", "nvfp4", "fp8_bf16head", "nvfp4_mse"])
+@pytest.mark.parametrize("variant", ["bf16", "fp8", "nvfp4", "fp8_bf16head", "nvfp4_mse", "nvfp4_all", "fp8_bf16scale"])
 def test_small_model_prompt_and_greedy(variant):
     master, model, om = make_pair(SMALL, variant, seed=31)
     prompt = S.prompt_ids(SMALL, 8)

@@ -85,6 +85,17 @@ def test_pack_nvfp4_scale_search_bit_exact(shape):
     assert np.array_equal(bs.cpu().numpy(), ob)
     assert np.array_equal(codes.cpu().numpy(), oc)
 
+
+@pytest.mark.parametrize("shape", [(67, 320), (1000, 3072), (151936, 1024)])
+def test_pack_fp8_bf16_scale_bit_exact(shape):
+    """bf16 row scales against the oracle, up to the full tied embedding / LM head."""
+    w = S.random_matrix(*shape, seed=26)
+    w[min(3, shape[0] - 1)] = 0
+    codes, scales = mk.pack_fp8_row(mk.upload_bf16(w), bf16_scale=True)
+    oc, os_ = O.quant_fp8_row(w, bf16_scale=True)
+    assert np.array_equal(scales.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
 def test_pack_full_size_lm_head_bit_exact():
     """The full 151,936 x 1024 tied matrix, FP8 per row, as the benchmark packs it."""
     w = S.random_matrix(151936, 1024, seed=23)

@@ -115,6 +115,24 @@ def test_quant_fp8_matches_torch_cast():
     assert np.array_equal(codes, ref_codes)
 
 
+
+def test_quant_fp8_bf16_scale_matches_torch_cast():
+    """bf16 row scales: torch's fp32 division, its bfloat16 cast of the scale, then its float8 cast
+    of w / scale clamped to the finite range (saturation), as library routines."""
+    w = S.random_matrix(67, 320, seed=8)
+    w[4, :] = 0
+    codes, scales = O.quant_fp8_row(w, bf16_scale=True)
+    wf = torch.from_numpy(w.view(np.int16)).view(torch.bfloat16).to(torch.float32)
+    s = (wf.abs().amax(dim=1) / torch.tensor(448.0)).to(torch.bfloat16).to(torch.float32)
+    q = torch.where(s[:, None] > 0, wf / s[:, None], torch.zeros_like(wf)).clamp(-448.0, 448.0)
+    assert np.array_equal(scales, s.numpy())
+    assert np.array_equal(codes, q.to(torch.float8_e4m3fn).view(torch.uint8).numpy())
+    # the scales are bf16 numbers; rows whose scale rounded down saturate their maximum at 448
+    assert np.array_equal(scales.view(np.uint32) & 0xFFFF, np.zeros(67, np.uint32))
+    fp32_s = (wf.abs().amax(dim=1) / torch.tensor(448.0)).numpy()
+    down = np.nonzero(scales < fp32_s)[0]
+    assert len(down) > 5 and all((codes[r] & 0x7F).max() == 0x7E for r in down)
+
 def test_quant_fp8_error_bound_and_zero_row():
     w = S.random_matrix(40, 256, seed=6)
     w[3, :] = 0

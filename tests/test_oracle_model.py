@@ -85,7 +85,7 @@ class TorchRef:
         return int(torch.argmax(logits)), logits.numpy()
 
 
-@pytest.mark.parametrize("variant", ["bf16", "fp8", "nvfp4", "fp8_bf16head", "nvfp4_mse"])
+@pytest.mark.parametrize("variant", ["bf16", "fp8", "nvfp4", "fp8_bf16head", "nvfp4_mse", "nvfp4_all", "fp8_bf16scale"])
 def test_oracle_matches_torch_composition(variant):
     master = S.master_weights(TINY, seed=11)
     packed = oracle_pack_model(master, S.format_map(variant))
