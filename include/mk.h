@@ -140,7 +140,8 @@ int mk_kv_cache(mk_model* m, int layer, void** k_dev, void** v_dev);
 int mk_debug_hidden(mk_model* m, float* out_dev);
 
 /* X-ray: copy the last step's trace (24-byte records: u64 globaltimer, u64 clock64, u32 smid,
- * u16 cta, u8 phase, u8 kind) into host_buf. Returns MK_ENOTRACE without MK_FLAG_XRAY. */
+ * u16 cta, u8 phase, u8 kind; one row of 2048 records per CTA, ended by a record of kind 255 where
+ * it is not full) into host_buf. Returns MK_ENOTRACE without MK_FLAG_XRAY. */
 int mk_trace_dump(mk_model* m, void* host_buf, size_t cap, size_t* written);
 
 /* Test hook: make CTA `cta` skip its signal after phase `phase` of layer 0 in the next steps, so

@@ -68,7 +68,7 @@ struct TraceRec {
   uint8_t phase;
   uint8_t kind;  // 0 = phase begin, 1 = phase end, 2 = wait begin, 3 = wait end
 };
-constexpr int TRACE_PER_CTA = 512;
+constexpr int TRACE_PER_CTA = 2048;
 
 // Activations cross SMs as 64-bit words {fp32 value (low), u32 tag (high)} stored with one
 // single-copy-atomic 64-bit store: a consumer polls the words themselves until every one carries

@@ -85,22 +85,34 @@ struct Sched {
   }
 };
 
+// One GEMV step of a layer (q/k/v, o_proj, gate/up, down_proj) or the LM head, as this CTA runs
+// it: everything about the step that does not change from layer to layer, filled once per launch.
+struct StepDesc {
+  const llword* src;  // LL input words
+  llword* ll;         // LL output base (the row index is added), null for the LM head
+  int r0, r1, K, nsrc;
+  int8_t mi, mbi;     // matrix indices into DLayer::m (-1: the tied embedding / LM head)
+  int8_t paired, normed, phase, wait_phase, epi, stag_m1, nwsel, fmt, nr, res;
+  int16_t ntiles;     // tiles of the step in format fmt (layer 0's format for the layer steps)
+};
+constexpr int NSTEPS = 6;  // QKV, (attention), O, gate/up, down, LM head
+
 struct __align__(16) Smem {
   uint64_t full[NSLOT];
   uint64_t empty[NSLOT];
   float xs[XS_MAX];
   float hs[HID];
-  float gs[64];
-  float us[64];
   float red[64];
   float qs[2][HD];
   float kn[HD];
   float vn[HD];
   float sc[2][UNIT_POS];
-  float stat[4];
   float wst[NCW][4];                 // attention: per-warp (max, sum) of both heads
   __align__(16) uint16_t knew[HD];   // attention: the new position's bf16 key and value rows
   __align__(16) uint16_t vnew[HD];
+  int2 geo[12];            // tile geometry per (format, K): rows per tile, division magic
+  StepDesc steps[NSTEPS];  // this CTA's GEMV steps
+  uint32_t wplan[NSTEPS][NCW][6];  // per step and warp: its first row group, tile-relative (plan_entry)
   DLayer lay[MAX_LAYERS];  // the layer table, copied once per launch
   Sched sched;             // this CTA's row ranges and attention unit
   int flag;
@@ -118,22 +130,14 @@ __device__ __forceinline__ int tile_rows(int fmt, int K) {
   int r = SLOT / (code_bytes(fmt, K) + scale_bytes(fmt, K));
   return r > 32 ? 32 : r;
 }
-// The same geometry as compile-time constants for the consumer's hot path: rows per tile, and the
-// multiplier m with i / rows == umulhi(i, m) for the row indices of one phase (i < 2^24).
-template <int FMT, int K>
-struct Geom {
-  static constexpr int CB = FMT == 0 ? 2 * K : (FMT == 1 ? K : K / 2);
-  static constexpr int SB = FMT == 2 ? K / 16 : 0;
-  static constexpr int RPT = SLOT / (CB + SB) > 32 ? 32 : SLOT / (CB + SB);
-  static constexpr uint32_t MAG = 0xFFFFFFFFu / (uint32_t)RPT + 1u;
-};
-template <int FMT>
-__device__ __forceinline__ void geom_of(int K, int& rpt, uint32_t& mag) {
-  switch (K) {
-    case 1024: rpt = Geom<FMT, 1024>::RPT, mag = Geom<FMT, 1024>::MAG; break;
-    case 2048: rpt = Geom<FMT, 2048>::RPT, mag = Geom<FMT, 2048>::MAG; break;
-    case 3072: rpt = Geom<FMT, 3072>::RPT, mag = Geom<FMT, 3072>::MAG; break;
-    default: rpt = Geom<FMT, 4096>::RPT, mag = Geom<FMT, 4096>::MAG; break;
+// The same geometry for the consumers, as a table in shared memory filled once per launch (one
+// shared-memory load instead of branches on the format and K): rows per tile, and the multiplier m
+// with i / rows == umulhi(i, m) for the row indices of one phase (i < 2^24). Entry fmt * 4 + K / 1024
+// - 1; K is a multiple of 1024 up to 4096.
+__device__ __forceinline__ void geo_fill(int2* geo, int t) {
+  if (t < 12) {
+    const int r = tile_rows(t / 4, 1024 * (t % 4 + 1));
+    geo[t] = make_int2(r, (int)(0xFFFFFFFFu / (uint32_t)r + 1u));
   }
 }
 // Position of input element k in the staged vector, laid out so that lane l of a warp reads the
@@ -166,6 +170,16 @@ struct Xray {
       r.phase = (uint8_t)phase;
       r.kind = (uint8_t)kind;
       base[n++] = r;
+    }
+  }
+  // Sub-phase mark (kind 4): the SM clock only (reading %globaltimer costs far more than clock64
+  // and would distort the short intervals the marks resolve); gtime = 0, smid = 0.
+  __device__ __forceinline__ void mark(int id) {
+    if (XR && base && n < TRACE_PER_CTA) {
+      unsigned long long* w = reinterpret_cast<unsigned long long*>(base + n++);
+      w[0] = 0ull;
+      w[1] = clock64_();
+      w[2] = ((unsigned long long)blockIdx.x << 32) | ((unsigned long long)(uint8_t)id << 48) | (4ull << 56);
     }
   }
   __device__ void finish() {
@@ -322,8 +336,8 @@ struct Consumer {
   __device__ __forceinline__ void st(int phase, int kind) {
     if (tid == 0) xr.stamp(phase, kind);
   }
-  __device__ __forceinline__ void mark(int id) {  // sub-phase stamp (kind 4), X-ray builds only
-    if (tid == 0) xr.stamp(id, 4);
+  __device__ __forceinline__ void mark(int id) {  // sub-phase mark (kind 4), X-ray builds only
+    if (tid == 0) xr.mark(id);
   }
   __device__ __forceinline__ bool faulted(int phase, int layer) const {
     return P->fault_cta == (int)blockIdx.x && P->fault_phase == phase && layer == 0;
@@ -332,7 +346,7 @@ struct Consumer {
   // going to the next CTA barrier, where the abort is seen by every warp).
   __device__ void wait_full(uint32_t slot, uint32_t par, int phase, int layer) {
     if (mbar_test_wait(&s->full[slot], par)) return;
-    if (XR && warp == 0 && lane == 0) xr.stamp(54, 4);  // X-ray: a tile was not there yet
+    if (XR && warp == 0 && lane == 0) xr.mark(54);  // X-ray: a tile was not there yet
     uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s->full[slot], par)) {  // suspends the warp for a while in hardware
       if (s->abort) return;
@@ -342,23 +356,38 @@ struct Consumer {
       }
     }
   }
-  // Wait for the n LL words at src (tag), two per thread per round, and stage them:
+  // Resident phases: every tile of the phase fits the ring at once, so warp 0 (lane i: the phase's
+  // tile i) waits for all of them to land while the CTA waits for its input anyway; the CTA barrier
+  // that publishes the staged input then publishes the tiles too, and the GEMV itself never waits.
+  __device__ __forceinline__ void resident_wait(int ntiles) {
+    if (warp == 0 && lane < ntiles) wait_full((n + lane) % NSLOT, ((n + lane) / NSLOT) & 1, PH_WAIT, -1);
+  }
+  // Tiles a GEMV phase of nrows rows (FFN units when paired) streams through the ring.
+  __device__ __forceinline__ int phase_tiles(int fmt, int K, int nrows, bool paired) const {
+    if (nrows <= 0) return 0;
+    int rpt;
+    uint32_t mag;
+    geom_rt(fmt, K, rpt, mag);
+    return (paired ? 2 : 1) * (int)__umulhi((uint32_t)(nrows + rpt - 1), mag);
+  }
+  // Wait for the nwords LL words at src (tag), two per thread per round, and stage them:
   //  normed: hs[k] = h[k], xs[k] = h[k] * w[k] (w = this thread's two bf16 norm weights of elements
   //          2 tid, 2 tid + 1, loaded before the wait), and red[warp] = the warp's sum of h^2;
   //  plain:  xs[k] = x[k].
   // xs is laid out for a matrix of format fmt. hook() runs before the closing CTA barrier.
   template <class Hook>
-  __device__ bool poll_stage(const llword* src, int n, uint32_t tag, int phase, int layer, bool normed, uint2 wb,
-                             int fmt, Hook hook) {
+  __device__ bool poll_stage(const llword* src, int nwords, uint32_t tag, int phase, int layer, bool normed, uint2 wb,
+                             int fmt, int res_tiles, Hook hook) {
     if (tid == 0) xr.stamp(phase, 2);
     const int epl = epl_of(fmt);
     constexpr int MAXW = (FFN + 2 * NCT - 1) / (2 * NCT);  // word pairs per thread, at most
-    const int nw = (n - 2 * tid + 2 * NCT - 1) / (2 * NCT);
+    const int nw = (nwords - 2 * tid + 2 * NCT - 1) / (2 * NCT);
     llword a[MAXW], b[MAXW];
     // every load of this thread goes out at once; only the late ones are polled again
 #pragma unroll
     for (int i = 0; i < MAXW; ++i)
       if (i < nw) ld_ll2(src + 2 * tid + 2 * NCT * i, a[i], b[i]);
+    resident_wait(res_tiles);  // overlaps the loads in flight
     bool ready = true;
 #pragma unroll
     for (int i = 0; i < MAXW; ++i)
@@ -387,6 +416,7 @@ struct Consumer {
         }
       }
     }
+    mark(47);
     float ss = 0.f;
 #pragma unroll
     for (int i = 0; i < MAXW; ++i) {
@@ -429,6 +459,14 @@ struct Consumer {
 #pragma unroll
     for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
     if (lane == 0) s->red[warp] = ss;
+  }
+  // This thread's two bf16 norm weights (elements 2 tid, 2 tid + 1 and 2 (tid + NCT), +1), as the
+  // staging reads them.
+  __device__ __forceinline__ uint2 load_norm(const uint16_t* w) const {
+    uint2 r = make_uint2(0u, 0u);
+    r.x = __ldg(reinterpret_cast<const uint32_t*>(w) + tid);
+    if (2 * (tid + NCT) < HID) r.y = __ldg(reinterpret_cast<const uint32_t*>(w) + tid + NCT);
+    return r;
   }
   // 1 / sqrt(mean(h^2) + eps) from the per-warp sums in red[] (after a CTA barrier).
   __device__ __forceinline__ float rms_inv() const {
@@ -493,6 +531,7 @@ struct Consumer {
       for (int ch = 0; ch < NCH; ++ch) body(ch, &xr[ch * Q]);
     } else {
       const float4* xs4 = reinterpret_cast<const float4*>(s->xs) + lane;
+#pragma unroll 2
       for (int ch = 0; ch < nchunk; ++ch) {
         float4 x[Q];
 #pragma unroll
@@ -504,6 +543,8 @@ struct Consumer {
     for (int r = 0; r < NR; ++r) out[r] = acc[r][0] + acc[r][1];
   }
 
+  // The steps of a layer, then the LM head.
+  enum { ST_QKV = 0, ST_ATTN, ST_O, ST_GU, ST_DOWN, ST_HEAD };
   // Epilogue of a GEMV phase, chosen at run time (one code copy per format instead of one per
   // phase keeps the kernel small).
   enum EpiKind { EPI_QKV, EPI_RESID, EPI_HEAD, EPI_OUT, EPI_ACT };
@@ -561,10 +602,10 @@ struct Consumer {
   }
   // Rows per tile and the umulhi magic for a runtime (format, K): compile-time constants behind a
   // switch, so the hot path has no integer division.
-  __device__ __forceinline__ static void geom_rt(int fmt, int K, int& rpt, uint32_t& mag) {
-    if (fmt == 0) geom_of<0>(K, rpt, mag);
-    else if (fmt == 1) geom_of<1>(K, rpt, mag);
-    else geom_of<2>(K, rpt, mag);
+  __device__ __forceinline__ void geom_rt(int fmt, int K, int& rpt, uint32_t& mag) const {
+    const int2 g = s->geo[fmt * 4 + (K >> 10) - 1];
+    rpt = g.x;
+    mag = (uint32_t)g.y;
   }
   // This warp's first row group of a GEMV phase, prepared before the phase's input arrives: its
   // row pointers into the ring and its row scales (their loads overlap the wait). The tiles are
@@ -605,8 +646,82 @@ struct Consumer {
     }
   }
 
+  // ---------------------------------------------------------------- per-launch step tables
+  // The same plan, worked out once per launch: row k of this warp's first group of step d as
+  // tile (relative to the step's first tile, b rows included) | row in tile << 6 | rows of that
+  // tile << 11 | unit index << 17. Only the ring position and the layer's pointers change later.
+  __device__ uint32_t plan_entry(const StepDesc& d, int k) const {
+    const int nrows = d.r1 - d.r0;
+    const bool paired = d.paired;
+    const int NR = d.nr, UPG = paired ? NR / 2 : NR, TPU = paired ? 2 : 1;
+    const int g0 = UPG * warp;
+    if (k >= NR || nrows <= 0 || g0 >= nrows) return 0u;
+    int rpt;
+    uint32_t rmag;
+    geom_rt(d.fmt, d.K, rpt, rmag);
+    const int T = (int)__umulhi((uint32_t)(nrows + rpt - 1), rmag);
+    const int u = g0 + (paired ? (k >> 1) : k);
+    const int isb = paired && (k & 1);
+    const int uu = u < nrows ? u : g0;
+    const int tl = (int)__umulhi((uint32_t)uu, rmag);
+    const int rit = uu - tl * rpt;
+    const int nr = tl == T - 1 ? nrows - tl * rpt : rpt;
+    return (uint32_t)(TPU * tl + isb) | ((uint32_t)rit << 6) | ((uint32_t)nr << 11) | ((uint32_t)uu << 17);
+  }
+  // plan_first from the table (the layer's matrices must have the format the table was made for).
+  __device__ __forceinline__ void plan_fast(const StepDesc& d, int step, const DMat& ma, const DMat& mb, Plan& pl) {
+    const int NR = d.nr, UPG = d.paired ? NR / 2 : NR;
+    if (d.r1 - d.r0 <= UPG * warp) return;  // no rows for this warp
+    const int fmt = d.fmt;
+    const int cb = code_bytes(fmt, d.K), sb = scale_bytes(fmt, d.K);
+    const float* sca = reinterpret_cast<const float*>(ma.scale) + d.r0;
+    const float* scb = reinterpret_cast<const float*>(mb.scale) + d.r0;
+    const uint32_t* w = s->wplan[step][warp];
+#pragma unroll
+    for (int k = 0; k < 6; ++k) {
+      if (k < NR) {
+        const uint32_t ent = w[k];
+        const int rit = (int)((ent >> 6) & 31u), nr = (int)((ent >> 11) & 63u), row = (int)(ent >> 17);
+        const uint8_t* tile = ring + (size_t)((n + (ent & 63u)) % NSLOT) * SLOT;
+        pl.code[k] = tile + (size_t)rit * cb;
+        pl.bsc[k] = tile + (size_t)nr * cb + (size_t)rit * sb;
+        const bool isb = d.paired && (k & 1);
+        pl.sc[k] = fmt == 1 ? __ldg((isb ? scb : sca) + row) : (fmt == 2 ? (isb ? mb.tscale : ma.tscale) : 1.f);
+      }
+    }
+  }
+  // Step `step` of this CTA (q/k/v rows, o_proj rows, FFN units, down_proj rows, LM-head rows).
+  __device__ void make_step(int step, const KParams& p, const Sched& S, StepDesc& d) const {
+    d.paired = 0, d.mbi = -1, d.ll = nullptr, d.nwsel = 0, d.stag_m1 = 0;
+    if (step == ST_QKV) {
+      d.mi = (int8_t)(M_Q + S.qm), d.r0 = S.qr0, d.r1 = S.qr1, d.K = HID, d.phase = PH_QKV, d.normed = 1;
+      d.src = p.h_mlp, d.nsrc = HID, d.stag_m1 = 1, d.epi = EPI_QKV, d.ll = p.qkv + S.qbase, d.wait_phase = PH_DOWN;
+    } else if (step == ST_O) {
+      d.mi = M_O, d.r0 = S.o0, d.r1 = S.o1, d.K = QROWS, d.phase = PH_O, d.normed = 0;
+      d.src = p.att, d.nsrc = QROWS, d.epi = EPI_RESID, d.ll = p.h_attn, d.wait_phase = PH_ATTN;
+    } else if (step == ST_GU) {
+      d.mi = M_GATE, d.mbi = M_UP, d.paired = 1, d.r0 = S.j0, d.r1 = S.j1, d.K = HID, d.phase = PH_GATEUP;
+      d.normed = 1, d.src = p.h_attn, d.nsrc = HID, d.nwsel = 1, d.epi = EPI_ACT, d.ll = p.act + S.j0;
+      d.wait_phase = PH_O;
+    } else if (step == ST_DOWN) {
+      d.mi = M_DOWN, d.r0 = S.d0, d.r1 = S.d1, d.K = FFN, d.phase = PH_DOWN, d.normed = 0;
+      d.src = p.act, d.nsrc = FFN, d.epi = EPI_RESID, d.ll = p.h_mlp, d.wait_phase = PH_GATEUP;
+    } else {  // final RMSNorm + LM head
+      d.mi = -1, d.r0 = S.v0, d.r1 = S.v1, d.K = HID, d.phase = PH_HEAD, d.normed = 1;
+      d.src = p.h_mlp, d.nsrc = HID, d.stag_m1 = 1, d.nwsel = 2, d.epi = EPI_HEAD, d.wait_phase = PH_DOWN;
+    }
+    d.fmt = (int8_t)(d.mi < 0 ? p.embed.fmt : p.layers[0].m[d.mi].fmt);
+    d.nr = (int8_t)group_rows(d.paired, d.K, d.r1 - d.r0);
+    d.ntiles = (int16_t)phase_tiles(d.fmt, d.K, d.r1 - d.r0, d.paired);
+    d.res = step != ST_HEAD && d.ntiles <= NSLOT;
+  }
+
+  // res: the phase is resident (every tile landed before the staging barrier, see resident_wait):
+  // no waits inside, and each warp releases all of the phase's tiles at once at the end (lane i:
+  // tile i). Otherwise the tiles stream through the ring as described above (the LM head).
   template <int FMT, bool REGX, bool PAIRED, int NR>
-  __device__ void gemv_t(const DMat& ma, const DMat& mb, int r0, int r1, int K, const Plan& pl, const EpiCtx& e) {
+  __device__ void gemv_t(const DMat& ma, const DMat& mb, int r0, int r1, int K, const Plan& pl, const EpiCtx& e,
+                         bool res) {
     constexpr int EPL = FMT == 0 ? 8 : (FMT == 1 ? 16 : 32);
     constexpr int UPG = PAIRED ? NR / 2 : NR;  // units per group
     constexpr int TPU = PAIRED ? 2 : 1;        // tiles per block of rpt units
@@ -614,10 +729,11 @@ struct Consumer {
     const int cb = code_bytes(FMT, K), sbytes = scale_bytes(FMT, K);
     int rpt;
     uint32_t rmag;
-    geom_of<FMT>(K, rpt, rmag);
+    geom_rt(FMT, K, rpt, rmag);
     const int nrows = r1 - r0;
     const int T = (int)__umulhi((uint32_t)(nrows + rpt - 1), rmag);  // tile blocks
     const int ntiles = TPU * T;
+    mark(40);
     float4 xr[8];
     if constexpr (REGX) {
       const float4* xs4 = reinterpret_cast<const float4*>(s->xs) + lane;
@@ -636,8 +752,11 @@ struct Consumer {
         const int glast = min(g0 + UPG, nrows) - 1;
         const int ta = TPU * (int)__umulhi((uint32_t)g0, rmag);
         const int tb = TPU * (int)__umulhi((uint32_t)glast, rmag) + TPU - 1;
-        flush_tiles(released, ta);
-        warp_wait_tiles(ta, tb - ta + 1, PH_WAIT, -1);
+        if (!res) {
+          flush_tiles(released, ta);
+          warp_wait_tiles(ta, tb - ta + 1, PH_WAIT, -1);
+        }
+        if (b0 == 0) mark(41);
         if (b0 == 0) {  // the first group was prepared before the input arrived
 #pragma unroll
           for (int k = 0; k < NR; ++k) code[k] = pl.code[k], bsc[k] = pl.bsc[k], sc[k] = pl.sc[k];
@@ -662,11 +781,13 @@ struct Consumer {
         }
         float part[NR];
         dot_rows<FMT, REGX, NR>(code, bsc, nchunk, xr, part);
+        if (b0 == 0) mark(42);
 #pragma unroll
         for (int o = 16; o; o >>= 1) {
 #pragma unroll
           for (int k = 0; k < NR; ++k) part[k] += __shfl_xor_sync(0xffffffffu, part[k], o);
         }
+        if (b0 == 0) mark(43);
         // every lane holds every sum: lane j writes unit g0 + j (selects, no dynamic register index)
         if constexpr (PAIRED) {
           float g = part[0] * sc[0], up = part[1] * sc[1];
@@ -684,34 +805,40 @@ struct Consumer {
             if (lane == k) y = part[k] * sc[k];
           if (lane < UPG && g0 + lane < nrows) epi_row(e, r0 + g0 + lane, y);
         }
+        if (b0 == 0) mark(44);
       }
       const int gnext = g0 + UPG * NCW;  // this warp's next group
-      flush_tiles(released, gnext < nrows ? TPU * (int)__umulhi((uint32_t)gnext, rmag) : ntiles);
+      if (!res) flush_tiles(released, gnext < nrows ? TPU * (int)__umulhi((uint32_t)gnext, rmag) : ntiles);
     }
+    if (res) {
+      __syncwarp();
+      if (lane < ntiles) mbar_arrive(&s->empty[(n + lane) % NSLOT]);
+    }
+    mark(45);
     n += ntiles;
   }
   // Dispatch on format and group width (the one call site of the engine).
   __device__ void gemv(bool paired, const DMat& ma, const DMat& mb, int r0, int r1, int K, const Plan& pl,
-                       const EpiCtx& e) {
+                       const EpiCtx& e, bool res) {
     if (r0 >= r1) return;
     const int fmt = ma.fmt;
     const int nr = group_rows(paired, K, r1 - r0);
     if (paired) {
-      if (fmt == 0) gemv_t<0, true, true, 6>(ma, mb, r0, r1, K, pl, e);
-      else if (fmt == 1) gemv_t<1, true, true, 6>(ma, mb, r0, r1, K, pl, e);
-      else gemv_t<2, true, true, 6>(ma, mb, r0, r1, K, pl, e);
+      if (fmt == 0) gemv_t<0, true, true, 6>(ma, mb, r0, r1, K, pl, e, res);
+      else if (fmt == 1) gemv_t<1, true, true, 6>(ma, mb, r0, r1, K, pl, e, res);
+      else gemv_t<2, true, true, 6>(ma, mb, r0, r1, K, pl, e, res);
     } else if (K == 1024) {
-      if (fmt == 0) gemv_t<0, true, false, 4>(ma, mb, r0, r1, K, pl, e);
-      else if (fmt == 1) gemv_t<1, true, false, 4>(ma, mb, r0, r1, K, pl, e);
-      else gemv_t<2, true, false, 4>(ma, mb, r0, r1, K, pl, e);
+      if (fmt == 0) gemv_t<0, true, false, 4>(ma, mb, r0, r1, K, pl, e, res);
+      else if (fmt == 1) gemv_t<1, true, false, 4>(ma, mb, r0, r1, K, pl, e, res);
+      else gemv_t<2, true, false, 4>(ma, mb, r0, r1, K, pl, e, res);
     } else if (nr == 1) {
-      if (fmt == 0) gemv_t<0, false, false, 1>(ma, mb, r0, r1, K, pl, e);
-      else if (fmt == 1) gemv_t<1, false, false, 1>(ma, mb, r0, r1, K, pl, e);
-      else gemv_t<2, false, false, 1>(ma, mb, r0, r1, K, pl, e);
+      if (fmt == 0) gemv_t<0, false, false, 1>(ma, mb, r0, r1, K, pl, e, res);
+      else if (fmt == 1) gemv_t<1, false, false, 1>(ma, mb, r0, r1, K, pl, e, res);
+      else gemv_t<2, false, false, 1>(ma, mb, r0, r1, K, pl, e, res);
     } else {
-      if (fmt == 0) gemv_t<0, false, false, 4>(ma, mb, r0, r1, K, pl, e);
-      else if (fmt == 1) gemv_t<1, false, false, 4>(ma, mb, r0, r1, K, pl, e);
-      else gemv_t<2, false, false, 4>(ma, mb, r0, r1, K, pl, e);
+      if (fmt == 0) gemv_t<0, false, false, 4>(ma, mb, r0, r1, K, pl, e, res);
+      else if (fmt == 1) gemv_t<1, false, false, 4>(ma, mb, r0, r1, K, pl, e, res);
+      else gemv_t<2, false, false, 4>(ma, mb, r0, r1, K, pl, e, res);
     }
   }
 
@@ -993,7 +1120,12 @@ struct Consumer {
 
   __device__ void run(const KParams& p) {
     const int G = gridDim.x;
-    if (tid == 0) s->sched.make(p);  // published by the barrier after the embedding
+    if (tid < NSTEPS) {  // the schedule and the step table, published by the barrier after the embedding
+      Sched S0;
+      S0.make(p);
+      if (tid == 0) s->sched = S0;
+      if (tid != ST_ATTN) make_step(tid, p, S0, s->steps[tid]);
+    }
     const Sched& S = s->sched;
     // ---------------- embedding: h = row `token` of the tied matrix (every CTA, no wait)
     st(PH_EMBED, 0);
@@ -1025,16 +1157,23 @@ struct Consumer {
       }
     }
     bar_consumers(NCT);
+    // this warp's row groups of every step, tile-relative (read back by this warp only)
+    for (int i = lane; i < NSTEPS * 6; i += 32)
+      if (i / 6 != ST_ATTN) s->wplan[i / 6][warp][i % 6] = plan_entry(s->steps[i / 6], i % 6);
+    __syncwarp();
+    // norm weights of the first input RMSNorm and the first post-attention RMSNorm (each later one
+    // is loaded one layer ahead of its use)
+    uint2 wq = load_norm(s->lay[0].ln_in), wg = load_norm(s->lay[0].ln_post);
     st(PH_EMBED, 1);
     best = -INFINITY;
     besti = 0x7FFFFFFF;
     // One pass per (layer, step); the single GEMV and wait call sites keep one code copy each.
-    enum { ST_QKV = 0, ST_ATTN, ST_O, ST_GU, ST_DOWN, ST_HEAD };
     for (int l = 0; l <= p.n_layers; ++l) {
       const bool head = l == p.n_layers;
       const DLayer& L = s->lay[head ? 0 : l];
       const uint32_t tag = p.tagbase + (uint32_t)l;
       for (int step = head ? ST_HEAD : ST_QKV; step <= (head ? ST_HEAD : ST_DOWN); ++step) {
+        mark(59);
         if (step == ST_ATTN) {
           if (S.unit) {
             st(PH_ATTN, 0);
@@ -1043,67 +1182,62 @@ struct Consumer {
           }
           continue;
         }
-        // ---- describe the phase
-        DMat ma, mb;
-        int r0, r1, K, phase;
-        bool paired = false, normed;
-        const llword* src;
-        int nsrc;
-        uint32_t stag;
-        const uint16_t* nw = nullptr;
+        // ---- the step: everything that does not change with the layer comes from the table
+        const StepDesc& d = s->steps[step];
+        const DMat ma = d.mi < 0 ? p.embed : L.m[d.mi];
+        const DMat mb = d.paired ? L.m[d.mbi] : ma;
+        const int r0 = d.r0, r1 = d.r1, K = d.K, phase = d.phase;
+        const bool paired = d.paired, normed = d.normed;
         EpiCtx e;
+        e.kind = d.epi;
         e.tag = tag;
         e.inv = 1.f;
-        e.fout = nullptr;
-        e.dbg = nullptr;
-        if (step == ST_QKV) {
-          ma = L.m[M_Q + S.qm], r0 = S.qr0, r1 = S.qr1;
-          K = HID, phase = PH_QKV, normed = true;
-          src = p.h_mlp, nsrc = HID, stag = tag - 1, nw = L.ln_in;
-          e.kind = EPI_QKV, e.ll = p.qkv + S.qbase, e.skip = faulted(PH_QKV, l);
-        } else if (step == ST_O) {
-          ma = L.m[M_O], r0 = S.o0, r1 = S.o1;
-          K = QROWS, phase = PH_O, normed = false;
-          src = p.att, nsrc = QROWS, stag = tag;
-          e.kind = EPI_RESID, e.ll = p.h_attn, e.skip = faulted(PH_O, l);
-        } else if (step == ST_GU) {
-          ma = L.m[M_GATE], mb = L.m[M_UP], r0 = S.j0, r1 = S.j1;
-          K = HID, phase = PH_GATEUP, normed = true, paired = true;
-          src = p.h_attn, nsrc = HID, stag = tag, nw = L.ln_post;
-          e.kind = EPI_ACT, e.ll = p.act + S.j0, e.skip = faulted(PH_GATEUP, l);
-        } else if (step == ST_DOWN) {
-          ma = L.m[M_DOWN], r0 = S.d0, r1 = S.d1;
-          K = FFN, phase = PH_DOWN, normed = false;
-          src = p.act, nsrc = FFN, stag = tag;
-          e.kind = EPI_RESID, e.ll = p.h_mlp, e.skip = faulted(PH_DOWN, l);
-          e.dbg = p.hidden_dbg ? p.hidden_dbg + (size_t)(l + 1) * HID : nullptr;
-        } else {  // final RMSNorm + LM head
-          ma = p.embed, r0 = S.v0, r1 = S.v1;
-          K = HID, phase = PH_HEAD, normed = true;
-          src = p.h_mlp, nsrc = HID, stag = tag - 1, nw = p.final_norm;
-          e.kind = EPI_HEAD, e.ll = nullptr, e.skip = false, e.fout = p.logits;
-        }
-        if (!paired) mb = ma;
+        e.ll = d.ll;
+        e.skip = step != ST_HEAD && faulted(phase, l);
+        e.fout = step == ST_HEAD ? p.logits : nullptr;
+        e.dbg = (step == ST_DOWN && p.hidden_dbg) ? p.hidden_dbg + (size_t)(l + 1) * HID : nullptr;
         const int fmt = ma.fmt;
+        mark(56);
         // ---- everything that does not depend on this step's input happens before the wait:
         // this warp's first row group (tiles, row pointers, row scales) and the norm weights
         Plan pl;
-        if (r0 < r1) plan_first(paired, ma, mb, r0, r1, K, pl);
+        int ntiles;
+        bool res;
+        if (fmt == d.fmt && mb.fmt == d.fmt) {
+          plan_fast(d, step, ma, mb, pl);
+          ntiles = d.ntiles;
+          res = d.res;
+        } else {  // a layer whose formats differ from layer 0's
+          if (r0 < r1) plan_first(paired, ma, mb, r0, r1, K, pl);
+          ntiles = phase_tiles(fmt, K, r1 - r0, paired);
+          res = step != ST_HEAD && ntiles <= NSLOT;
+        }
+        mark(57);
+        // the norm weights were loaded a layer ago; load the next ones of the same kind now
         uint2 wb = make_uint2(0u, 0u);
         if (normed) {
-          wb.x = __ldg(reinterpret_cast<const uint32_t*>(nw) + tid);
-          if (2 * (tid + NCT) < HID) wb.y = __ldg(reinterpret_cast<const uint32_t*>(nw) + tid + NCT);
+          if (d.nwsel == 1) {
+            wb = wg;
+            if (l + 1 < p.n_layers) wg = load_norm(s->lay[l + 1].ln_post);
+          } else {
+            wb = wq;
+            if (d.nwsel == 0) wq = load_norm(l + 1 < p.n_layers ? s->lay[l + 1].ln_in : p.final_norm);
+          }
         }
+        mark(58);
         if (step == ST_QKV && l == 0) {  // the input is the embedding row already in hs
           stage_local(wb, fmt);
+          resident_wait(res ? ntiles : 0);
           bar_consumers(NCT);
-        } else if (!poll_stage(src, nsrc, stag, phase == PH_QKV || phase == PH_HEAD ? PH_DOWN : phase - 1, l,
-                               normed, wb, fmt, [] {})) {
+          if (s->abort) return;
+        } else if (!poll_stage(d.src, d.nsrc, tag - (uint32_t)d.stag_m1, d.wait_phase, l, normed, wb, fmt,
+                               res ? ntiles : 0, [] {})) {
           return;
         }
         st(phase, 0);
         if (normed) e.inv = rms_inv();
-        gemv(paired, ma, mb, r0, r1, K, pl, e);
+        gemv(paired, ma, mb, r0, r1, K, pl, e, res);
+        mark(46);
         bar_consumers(NCT);  // every warp is done with xs and hs before they are restaged
         st(phase, 1);
       }
@@ -1159,6 +1293,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_decode(const KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
   Smem* s = reinterpret_cast<Smem*>(smem_raw + RING_BYTES);
+  geo_fill(s->geo, threadIdx.x);
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&s->full[i], 1);
@@ -1192,6 +1327,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
   Smem* s = reinterpret_cast<Smem*>(smem_raw + RING_BYTES);
+  geo_fill(s->geo, threadIdx.x);
   if (threadIdx.x == 0) {
     for (int i = 0; i < NSLOT; ++i) {
       mbar_init(&s->full[i], 1);
@@ -1241,7 +1377,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
     e.dbg = nullptr;
     typename Consumer<false>::Plan pl;
     if (r0 < r1) c.plan_first(false, m, m, r0, r1, cols, pl);
-    c.gemv(false, m, m, r0, r1, cols, pl, e);
+    c.gemv(false, m, m, r0, r1, cols, pl, e, false);
     bar_consumers(NCT);
   }
 }

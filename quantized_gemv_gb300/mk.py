@@ -21,6 +21,7 @@ ERRNAMES = {MK_EINVAL: "MK_EINVAL", MK_ECUDA: "MK_ECUDA", MK_ETIMEOUT: "MK_ETIME
             MK_ENORESIDENT: "MK_ENORESIDENT", MK_ENOTRACE: "MK_ENOTRACE"}
 TRACE_DTYPE = np.dtype([("gtime", "<u8"), ("clk", "<u8"), ("smid", "<u4"), ("cta", "<u2"),
                         ("phase", "u1"), ("kind", "u1")])
+TRACE_PER_CTA = 2048  # records kept per CTA (the kernel's trace row length)
 PHASES = {0: "qkv", 1: "attention", 2: "o_proj", 3: "gate_up", 4: "down", 5: "lm_head", 6: "embed"}
 
 
@@ -286,12 +287,12 @@ class Model:
     def trace(self) -> np.ndarray:
         cap = 0
         grid = torch.cuda.get_device_properties(0).multi_processor_count
-        cap = grid * 512 * TRACE_DTYPE.itemsize
+        cap = grid * TRACE_PER_CTA * TRACE_DTYPE.itemsize
         buf = np.zeros(cap, dtype=np.uint8)
         written = C.c_size_t()
         self._err(lib().mk_trace_dump(self.h, buf.ctypes.data_as(C.c_void_p), cap, C.byref(written)), "mk_trace_dump")
         recs = buf[: written.value].view(TRACE_DTYPE)
-        return recs.reshape(len(recs) // 512, 512)  # one row of records per CTA of the grid
+        return recs.reshape(len(recs) // TRACE_PER_CTA, TRACE_PER_CTA)  # one row of records per CTA of the grid
 
     def debug_fault(self, cta: int, phase: int, timeout_ms: int = 0):
         self._err(lib().mk_debug_fault(self.h, cta, phase, timeout_ms), "mk_debug_fault")

@@ -19,17 +19,20 @@ import numpy as np
 
 PHASE_NAMES = {0: "qkv", 1: "attention", 2: "o_proj", 3: "gate_up", 4: "down", 5: "lm_head", 6: "embed"}
 GEMV_PHASES = (0, 2, 3, 4)
-KIND_BEGIN, KIND_END, KIND_WAIT_BEGIN, KIND_WAIT_END, KIND_STOP = 0, 1, 2, 3, 255
+KIND_BEGIN, KIND_END, KIND_WAIT_BEGIN, KIND_WAIT_END, KIND_MARK, KIND_STOP = 0, 1, 2, 3, 4, 255
 
 
 def records(trace: np.ndarray):
-    """Yield (cta, [(t_ns, phase, kind), ...]) for every CTA that wrote records."""
+    """Yield (cta, [(t_ns, phase, kind), ...]) for every CTA that wrote records (phase and wait
+    stamps; sub-phase marks, which carry only the SM clock, are left out)."""
     for cta in range(trace.shape[0]):
         rows = trace[cta]
         out = []
         for r in rows:
             if r["kind"] == KIND_STOP or (r["gtime"] == 0 and r["kind"] == 0 and r["phase"] == 0):
                 break
+            if r["kind"] == KIND_MARK:
+                continue
             out.append((int(r["gtime"]), int(r["phase"]), int(r["kind"])))
         if out:
             yield cta, out
