@@ -1,0 +1,100 @@
+"""X-ray: the analyser on a hand-built trace (CPU), and the instrumented build on the GPU (same
+tokens and logits as the plain build, well-formed per-CTA records)."""
+import numpy as np
+import pytest
+import torch
+
+from quantized_gemv_gb300 import xray
+
+TRACE_DTYPE = np.dtype([("gtime", "<u8"), ("clk", "<u8"), ("smid", "<u4"), ("cta", "<u2"),
+                        ("phase", "u1"), ("kind", "u1")])
+B, E, WB, WE, MARK, STOP = 0, 1, 2, 3, 4, 255
+QKV, ATT, O, GU, DOWN, HEAD, EMBED = 0, 1, 2, 3, 4, 5, 6
+
+
+def _trace(rows_per_cta, width=64):
+    tr = np.zeros((len(rows_per_cta), width), dtype=TRACE_DTYPE)
+    for c, rows in enumerate(rows_per_cta):
+        for i, (t, ph, kind) in enumerate(rows + [(0, 0, STOP)]):
+            tr[c][i] = (t, 7 * t, 3, c, ph, kind)
+    return tr
+
+
+def _one_layer(t0, wait_before_o):
+    """Records of one CTA for one layer (ns from t0) with a sub-phase mark that carries no time."""
+    return [(t0, QKV, B), (0, 40, MARK), (t0 + 100, QKV, E),
+            (t0 + 100, ATT, WB), (t0 + 100 + wait_before_o, ATT, WE), (t0 + 110 + wait_before_o, O, B),
+            (t0 + 160 + wait_before_o, O, E), (t0 + 160 + wait_before_o, O, WB), (t0 + 170 + wait_before_o, O, WE),
+            (t0 + 170 + wait_before_o, GU, B), (t0 + 250 + wait_before_o, GU, E),
+            (t0 + 250 + wait_before_o, GU, WB), (t0 + 260 + wait_before_o, GU, WE),
+            (t0 + 260 + wait_before_o, DOWN, B), (t0 + 300 + wait_before_o, DOWN, E)]
+
+
+def test_analyze_hand_trace():
+    a = [(1000, EMBED, B), (1010, EMBED, E)] + _one_layer(1010, 40) + [(1350, DOWN, WB), (1360, DOWN, WE),
+                                                                       (1360, HEAD, B), (1500, HEAD, E)]
+    b = [(1005, EMBED, B), (1012, EMBED, E)] + _one_layer(1012, 20) + [(1332, DOWN, WB), (1340, DOWN, WE),
+                                                                       (1340, HEAD, B), (1480, HEAD, E)]
+    tr = _trace([a, b])
+    # marks (kind 4, gtime 0) are not phase records
+    assert all(k != MARK for _, recs in xray.records(tr) for _, _, k in recs)
+    r = xray.analyze(tr)
+    assert r["ctas"] == 2
+    assert r["token_ns"] == 1500 - 1000
+    # waits: CTA a 40 + 10 + 10 + 10 = 70, CTA b 20 + 10 + 10 + 8 = 48
+    assert r["barrier_wait_ns"] == pytest.approx((70 + 48) / 2)
+    # GEMV phases: qkv 100 + o 50 + gu 80 + down 40 = 270 for both
+    assert r["weight_read_ns"] == pytest.approx(270)
+    assert r["lm_head_ns"] == pytest.approx((140 + 140) / 2)
+    # idle: a ends last (1500); b ends at 1480
+    assert r["idle_ns"] == pytest.approx(10)
+    assert xray.layer_timeline(tr) == []  # one layer: no layer-to-layer interval
+
+
+@pytest.mark.gpu
+def test_instrumented_build_matches_plain_build():
+    from quantized_gemv_gb300 import mk
+    from quantized_gemv_gb300 import synthetic as S
+
+    cfg = S.ModelConfig(n_layers=2, vocab=4099, max_ctx=256)
+    master = S.master_weights(cfg, seed=61)
+    packed = mk.pack_model(master, S.format_map("fp8"))
+    plain = mk.Model(cfg, packed)
+    xr = mk.Model(cfg, packed, flags=mk.MK_FLAG_XRAY)
+    tok = 3
+    for pos in range(6):  # teacher-forced on the plain build's tokens
+        lp = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+        lx = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+        nxt = plain.decode_step(tok, pos, lp)
+        nxt_x = xr.decode_step(tok, pos, lx)
+        # the same arithmetic in both builds (a different compilation may contract differently)
+        assert torch.allclose(lp, lx, rtol=0, atol=1e-4)
+        top2 = torch.topk(lp, 2).values
+        assert nxt_x == nxt or float(top2[0] - top2[1]) < 1e-3
+        tok = nxt
+    tr = xr.trace()
+    grid = mk.decode_grid()
+    assert tr.shape == (grid, mk.TRACE_PER_CTA)
+    written = []
+    for c in range(grid):
+        stop = np.flatnonzero(tr[c]["kind"] == STOP)
+        assert len(stop) > 0, c  # every CTA ended its row (the rest of the buffer is not this step's)
+        written.append(tr[c][: stop[0]])
+    written = np.concatenate(written)
+    assert set(np.unique(written["kind"]).tolist()) <= {B, E, WB, WE, MARK}
+    marks = written[written["kind"] == MARK]
+    assert len(marks) > 0 and np.all(marks["gtime"] == 0) and np.all(marks["clk"] > 0)
+    for cta, recs in xray.records(tr):
+        begins = [ph for _, ph, k in recs if k == B]
+        # every CTA runs the four GEMV phases of each layer, then the LM head
+        for ph in (QKV, O, GU, DOWN):
+            assert begins.count(ph) == cfg.n_layers, (cta, ph)
+        assert begins.count(HEAD) == 1
+        ts = [t for t, _, _ in recs]
+        assert ts == sorted(ts)
+    r = xray.analyze(tr)
+    assert r["ctas"] == grid
+    for k in ("weight_read_ns", "barrier_wait_ns", "lm_head_ns"):
+        assert 0 <= r[k] <= r["token_ns"]
+    plain.close()
+    xr.close()
