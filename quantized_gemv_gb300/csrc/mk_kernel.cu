@@ -3,13 +3,13 @@
 //
 // Structure (per CTA, one CTA per SM):
 //   * a producer warp streams this CTA's weight rows (and, for attention units, its slice of the
-//     bf16 KV cache) with cp.async.bulk into an 11-slot shared-memory ring. Weights do not depend
+//     bf16 KV cache) with cp.async.bulk into a 12-slot shared-memory ring. Weights do not depend
 //     on the token, so the stream runs ahead across every wait ("productive spin", monolith page,
 //     "Upstream facts"; generalised from an L2 prefetch into staging in the SM's own memory);
-//   * 16 consumer warps each own whole rows: they dequantise the staged rows in registers (cvt
+//   * 8 consumer warps each own whole rows: they dequantise the staged rows in registers (cvt
 //     e4m3x2 / e2m1x2 -> f16x2 -> fp32), keep the activation slice of a lane in registers, and
-//     accumulate in fp32 with one warp-shuffle reduction per row; warps take and release ring
-//     slots independently, so no CTA barrier sits inside a phase;
+//     accumulate in fp32 with one warp-shuffle reduction per row; a layer phase's tiles are all
+//     resident before it starts (the LM head streams), so no CTA barrier sits inside a phase;
 //   * grid barriers are replaced by per-element readiness: every activation crosses SMs as a
 //     64-bit {value, tag} word and a consumer waits only on the words it reads (the counter idea
 //     of "Hazy-style counters", monolith page, "Design decisions", sync experiment 2, with the
