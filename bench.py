@@ -260,8 +260,12 @@ def stream_read_gbs(mk):
     return n / (best * 1e-3) / 1e9
 
 
-def oracle_sample(wl: S.Workload, master, seconds: float = 12.0):
-    """The CPU oracle decoding the same workload on this host's cores: steps until `seconds`."""
+def oracle_sample(wl: S.Workload, master, seconds: float = 12.0, steps: int | None = None, warmup: int = 0,
+                  budget_s: float = 150.0):
+    """The CPU oracle decoding the same workload on this host's cores, at the positions the GPU arm
+    times: the prompt (or the prefilled KV cache) first, untimed, then `warmup` untimed greedy
+    steps, then timed greedy steps: `steps` of them, or as many as fit in `seconds` when steps is
+    None, and never more than fit in `budget_s` (the sample says how many were timed)."""
     from oracle import oracle as O
     cfg = wl.config()
     cores = len(os.sched_getaffinity(0))
@@ -272,17 +276,30 @@ def oracle_sample(wl: S.Workload, master, seconds: float = 12.0):
         om.set_kv(k, v)
         pos, tok = wl.prefill, int(S.prompt_ids(cfg, 1)[0])
     else:
-        pos, tok = 0, int(S.prompt_ids(cfg, 1)[0])
-    steps, t0 = 0, time.perf_counter()
+        prompt = S.prompt_ids(cfg, wl.prompt_len)
+        tok = int(prompt[0])
+        for pos in range(wl.prompt_len):
+            nxt, _, _, _ = om.step(tok, pos, want_logits=False)
+            tok = int(prompt[pos + 1]) if pos + 1 < wl.prompt_len else nxt
+        pos = wl.prompt_len
+    for _ in range(max(warmup, 0)):
+        tok, _, _, _ = om.step(tok, pos, want_logits=False)
+        pos += 1
+    first, n, t0 = pos, 0, time.perf_counter()
     while True:
         tok, _, _, _ = om.step(tok, pos, want_logits=False)
         pos += 1
-        steps += 1
+        n += 1
         el = time.perf_counter() - t0
-        if el >= seconds and steps >= 2:
+        if steps is not None and n >= steps:
             break
-    return {"value": steps / el, "unit": "tok/s", "cores": cores, "kind": "oracle",
-            "sample": f"{steps} greedy steps of {wl.name} from position {0 if not wl.prefill else wl.prefill} "
+        if steps is None and el >= seconds and n >= 2:
+            break
+        if el >= budget_s and n >= 2:
+            break
+    return {"value": n / el, "unit": "tok/s", "cores": cores, "kind": "oracle", "steps": n,
+            "sample": f"{n} timed greedy steps of {wl.name} at positions {first}..{pos - 1} after "
+                      f"{'the prefilled KV' if wl.prefill else 'the prompt'} and {max(warmup, 0)} untimed steps "
                       f"({el:.1f} s, double precision, {cores} threads)"}
 
 
@@ -410,9 +427,10 @@ def main():
         if rank != 0:
             return
         master = S.master_weights(wl.config(), seed=0)
-        cb = oracle_sample(wl, master, seconds=20.0)
+        cb = oracle_sample(wl, master, steps=args.steps, warmup=args.warmup)
         line = {"metric": "batch-1 decode tok/s (Qwen3-0.6B shape)", "value": cb["value"], "unit": "tok/s",
-                "impl": "reference", "n_gpus": 0, "steps": None, "warmup": 0, "higher_is_better": True,
+                "impl": "reference", "device": "host cpu", "n_gpus": args.gpus, "steps": cb["steps"],
+                "warmup": args.warmup, "higher_is_better": True,
                 "dtype": "f64", "data": "synthetic (seeded random weights, uniform prompt ids)",
                 "config": {"workload": wl.name, "description": wl.description},
                 "cpu_baseline": cb, "e2e": {"value": cb["value"], "unit": "tok/s", "h2d_bytes_per_step": 0,
