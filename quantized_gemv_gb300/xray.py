@@ -13,6 +13,7 @@ finishes).
 """
 from __future__ import annotations
 
+import gzip
 import json
 
 import numpy as np
@@ -111,10 +112,23 @@ def layer_timeline(trace: np.ndarray) -> list:
 
 
 def export_json(trace: np.ndarray, path: str, meta: dict | None = None):
-    """Compact JSON of one token's trace: one list of [t_ns, phase, kind] per CTA (t from token start)."""
+    """Compact JSON of one token's trace: one list of [t_ns, phase, kind] per CTA (t from token start),
+    gzip-compressed when the path ends in .gz."""
     per = dict(records(trace))
     t0 = min(r[0][0] for r in per.values())
     doc = {"meta": meta or {}, "phases": PHASE_NAMES,
            "ctas": {str(c): [[t - t0, ph, k] for t, ph, k in recs] for c, recs in per.items()}}
-    with open(path, "w") as f:
-        json.dump(doc, f, separators=(",", ":"))
+    text = json.dumps(doc, separators=(",", ":"))
+    if path.endswith(".gz"):
+        with gzip.open(path, "wt") as f:
+            f.write(text)
+    else:
+        with open(path, "w") as f:
+            f.write(text)
+
+
+def load_json(path: str) -> dict:
+    """Read back what export_json wrote."""
+    opener = gzip.open if path.endswith(".gz") else open
+    with opener(path, "rt") as f:
+        return json.load(f)

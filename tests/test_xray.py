@@ -98,3 +98,30 @@ def test_instrumented_build_matches_plain_build():
         assert 0 <= r[k] <= r["token_ns"]
     plain.close()
     xr.close()
+
+
+@pytest.mark.parametrize("suffix", [".json", ".json.gz"])
+def test_export_round_trip(tmp_path, suffix):
+    a = [(1000, EMBED, B), (1010, EMBED, E)] + _one_layer(1010, 40)
+    b = [(1005, EMBED, B), (1012, EMBED, E)] + _one_layer(1012, 20)
+    tr = _trace([a, b])
+    path = str(tmp_path / ("trace" + suffix))
+    xray.export_json(tr, path, meta={"workload": "hand-built"})
+    doc = xray.load_json(path)
+    assert doc["meta"] == {"workload": "hand-built"}
+    assert sorted(doc["ctas"]) == ["0", "1"]
+    # times are relative to the first record of the token; marks are not exported
+    assert doc["ctas"]["0"][0] == [0, EMBED, B]
+    assert doc["ctas"]["1"][0] == [5, EMBED, B]
+    assert len(doc["ctas"]["0"]) == len(a) - 1
+    assert all(k != MARK for recs in doc["ctas"].values() for _, _, k in recs)
+
+
+def test_layer_timeline_two_layers():
+    # two layers: the interval between the last CTA's ends of down_proj
+    a = _one_layer(100, 40) + _one_layer(500, 40)
+    b = _one_layer(110, 20) + _one_layer(480, 20)
+    tr = _trace([a, b])
+    # CTA a ends down_proj at 440 and 840, CTA b at 430 and 800 (an all-zero record ends a row, so
+    # no record sits at time 0)
+    assert xray.layer_timeline(tr) == [840 - 440]
