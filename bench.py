@@ -43,7 +43,8 @@ sys.path.insert(0, ROOT)
 from quantized_gemv_gb300 import synthetic as S  # noqa: E402
 
 HEADLINE = "qwen3_0.6b_bf16"
-UPSTREAM_BF16_TOKS = 1033.0  # RTX 5090 upstream kernel, bf16 (monolith page, "Upstream facts")
+UPSTREAM_BF16_TOKS = 1033.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (about 8 TB/s); the roofline divides by the measured copy  # RTX 5090 upstream kernel, bf16 (monolith page, "Upstream facts")
 
 
 # ------------------------------------------------------------------ byte accounting
@@ -462,6 +463,7 @@ def main():
                               "weight_gbs": round(r2["weight_gbs"], 1),
                               "roofline_frac_weights": round(r2["weight_gbs"] / peak, 4),
                               "roofline_frac_weights_kv": round(r2["total_gbs"] / peak, 4),
+                              "frac_of_nominal_weights_kv": round(r2["total_gbs"] / NOMINAL_HBM_GBS, 4),
                               "e2e_tok_s": round(r2["e2e_tok_s"], 1), "clocks": r2["clocks"]}
     xr = None
     if rank == 0 and not args.no_xray and not wl.prefill:
@@ -488,7 +490,9 @@ def main():
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl.name),
                      "kernel": "mk::k_decode", "peak_kind": f"{peak_kind} copy bandwidth (MEASURED_PEAKS.json hbm_gbs)",
                      "algorithmic_bytes_per_launch": res["weight_bytes"] + res["kv_bytes"],
-                     "launch_ms": round(res["launch_ms"], 5)},
+                     "launch_ms": round(res["launch_ms"], 5),
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "nominal_peak": NOMINAL_HBM_GBS},
         "stream_read_gbs": round(stream_gbs, 1) if stream_gbs else None,
         "cpu_baseline": cpu,
         "e2e": {"value": round(res["e2e_tok_s"], 2), "unit": "tok/s", "h2d_bytes_per_step": 4,
