@@ -317,13 +317,16 @@ def xray_summary(wl: S.Workload, mk, master, steps: int = 16):
         nxt = model.decode_step(tok, pos)
         tok = int(prompt[pos + 1]) if pos + 1 < wl.prompt_len else nxt
     total_ms, _, _ = time_steps(model, tok, wl.prompt_len, steps, 2)
-    a = xray.analyze(model.trace())
+    tr = model.trace()
+    a = xray.analyze(tr)
+    cp = xray.critical_path(tr)
     model.close()
     t = a["token_ns"]
     return {"token_us": round(t / 1e3, 1), "ctas": a["ctas"],
             "weight_read_share": round(a["weight_read_ns"] / t, 3), "barrier_wait_share": round(a["barrier_wait_share"], 3),
             "attention_share": round(a["attention_ns"] / t, 3), "lm_head_share": round(a["lm_head_ns"] / t, 3),
             "instrumented_tok_s": round(steps / (total_ms * 1e-3), 1),
+            "critical_path_us": {k: round(v / 1e3, 3) for k, v in cp.items() if k != "layers"},
             "note": "one instrumented step at the end of a 16-step greedy run; shares of the token's wall time, "
                     "averaged over CTAs"}
 

@@ -132,3 +132,47 @@ def load_json(path: str) -> dict:
     opener = gzip.open if path.endswith(".gz") else open
     with opener(path, "rt") as f:
         return json.load(f)
+
+
+def critical_path(trace: np.ndarray) -> dict:
+    """Per layer, where the dependent chain spends its time (ns, means over layers 1..L-2 so that
+    the first and last layers' set-up and tail do not distort them).
+
+    For each GEMV phase P of a layer: `phase_<P>` is the span from the last CTA's end of waiting for
+    P's input to the last CTA's end of P (the phase on the critical path); `exchange_<P>` is the span
+    from the last CTA's end of the phase that produces P's input to the first and the last CTA's end
+    of waiting for it (hop, polling and staging; the two ends bound the spread between CTAs). The
+    attention of a layer sits inside `exchange_o_proj`, since o_proj waits for its outputs.
+    """
+    prev_of = {0: 4, 2: 0, 3: 2, 4: 3}  # producing phase of each GEMV phase's input (QKV <- down)
+    ends = {}      # (layer, phase) -> list of end times
+    waits = {}     # (layer, consumer phase) -> list of wait-end times
+    for _, recs in records(trace):
+        layer, open_wait_for = 0, None
+        for t, ph, kind in recs:
+            if kind == KIND_END and ph in (0, 2, 3, 4):
+                ends.setdefault((layer, ph), []).append(t)
+                if ph == 4:
+                    layer += 1
+            elif kind == KIND_WAIT_END and ph in (1, 2, 3, 4):
+                # a wait is stamped with the phase that produces the input: 1 -> o_proj, 2 -> gate_up,
+                # 3 -> down, 4 -> the next layer's QKV (or the LM head)
+                consumer = {1: 2, 2: 3, 3: 4, 4: 0}[ph]
+                waits.setdefault((layer, consumer), []).append(t)
+    n_layers = max((l for (l, p) in ends if p == 4), default=-1) + 1
+    acc = {}
+    for l in range(1, n_layers - 1):
+        for ph, name in ((0, "qkv"), (2, "o_proj"), (3, "gate_up"), (4, "down")):
+            w = waits.get((l, ph))
+            e = ends.get((l, ph))
+            src = ends.get((l - 1 if ph == 0 else l, prev_of[ph]))
+            if not w or not e or not src:
+                continue
+            acc.setdefault("phase_" + name, []).append(max(e) - max(w))
+            acc.setdefault("exchange_" + name + "_first", []).append(min(w) - max(src))
+            acc.setdefault("exchange_" + name + "_last", []).append(max(w) - max(src))
+    out = {k: float(np.mean(v)) for k, v in acc.items()}
+    lt = layer_timeline(trace)
+    out["layer"] = float(np.mean(lt[1:-1])) if len(lt) > 2 else (float(np.mean(lt)) if lt else 0.0)
+    out["layers"] = n_layers
+    return out

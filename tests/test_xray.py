@@ -125,3 +125,25 @@ def test_layer_timeline_two_layers():
     # CTA a ends down_proj at 440 and 840, CTA b at 430 and 800 (an all-zero record ends a row, so
     # no record sits at time 0)
     assert xray.layer_timeline(tr) == [840 - 440]
+
+
+def test_critical_path_three_layers():
+    # three identical layers per CTA, 400 ns apart; CTA b is 10 ns behind CTA a everywhere
+    a = [(1000, EMBED, B), (1010, EMBED, E)]
+    b = [(1000, EMBED, B), (1012, EMBED, E)]
+    for l in range(3):
+        t0 = 1100 + 400 * l
+        a += ([(t0 - 20, DOWN, WB), (t0 - 5, DOWN, WE)] if l else []) + _one_layer(t0, 40)
+        b += ([(t0 - 15, DOWN, WB), (t0 + 5, DOWN, WE)] if l else []) + _one_layer(t0 + 10, 40)
+    tr = _trace([a, b], width=128)
+    cp = xray.critical_path(tr)
+    assert cp["layers"] == 3
+    # layer 1 (t0 = 1500): o_proj's wait ends at t0 + 140 (a) and t0 + 150 (b); its phase ends at
+    # t0 + 200 / t0 + 210; QKV ends at t0 + 100 / t0 + 110
+    assert cp["phase_o_proj"] == 210 - 150
+    assert cp["exchange_o_proj_first"] == 140 - 110
+    assert cp["exchange_o_proj_last"] == 150 - 110
+    # QKV of layer 1 waits for layer 0's down_proj (ends 1100 + 340 and 1110 + 340)
+    assert cp["exchange_qkv_last"] == (1500 + 5) - (1110 + 340)
+    assert cp["phase_qkv"] == (1510 + 100) - (1500 + 5)
+    assert cp["layer"] == 400
