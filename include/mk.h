@@ -2,8 +2,8 @@
  * transformers on NVIDIA GB300 (sm_103a).
  *
  * One call of mk_decode_step runs ONE persistent kernel that executes every layer and the
- * LM-head argmax, so one launch produces one token ("One kernel per token", monolith page,
- * "Why it's exciting"; "fold the LM head and argmax into the megakernel", monolith page,
+ * LM-head argmax, so one launch produces one token (monolith page, "Why it's exciting", first
+ * bullet: a single persistent launch per decode step, with the upstream LM-head kernels folded in;
  * "Design decisions", sync experiment 5).
  *
  * Conventions for every entry point below:
@@ -69,8 +69,8 @@ typedef struct {
   const void *ln_in, *ln_post, *q_norm, *k_norm;
 } mk_layer;
 
-/* The tied embedding / LM-head matrix [vocab][hidden] is MK_BF16 or MK_FP8_ROW (the LM head
- * stays FP8 in the NVFP4 variant: "The LM head stays FP8", monolith page, NVFP4 format). */
+/* The tied embedding / LM-head matrix [vocab][hidden] is MK_BF16 or MK_FP8_ROW (the NVFP4 variant
+ * keeps its LM head in FP8: monolith page, "Design decisions", NVFP4 format). */
 typedef struct {
   const mk_layer* layers; /* host array of n_layers entries (copied by mk_create) */
   mk_mat embed;
@@ -94,7 +94,9 @@ int mk_decode_grid(void);
 
 /* Bytes of device workspace a model needs: bf16 KV cache [n_layers][n_kv][max_ctx][head_dim] for
  * keys and for values, a RoPE cos/sin table, activations, sync counters, an optional per-layer
- * hidden-state buffer and, with MK_FLAG_XRAY, the trace buffer. Returns 0 on a bad config. */
+ * hidden-state buffer and, with MK_FLAG_XRAY, the trace buffer. Returns 0 on a bad config.
+ * An addition of this library (the pages have no counterpart): it lets the caller own every
+ * device allocation. */
 size_t mk_workspace_bytes(const mk_config* cfg, unsigned flags);
 
 /* Validate the config and weights, lay out the caller's zeroed-or-not workspace (it is cleared
@@ -132,16 +134,25 @@ int mk_decode_next(mk_model* m, const int32_t* token_dev, int32_t pos, int32_t* 
 int mk_sync(mk_model* m);
 
 /* Device pointers to layer `layer`'s bf16 K and V caches, each [n_kv_heads][max_ctx][head_dim],
- * for prefilling or inspecting the cache. */
+ * for prefilling or inspecting the cache. An addition of this library (the pages have no
+ * counterpart); the cache itself is kept in bf16 as the monolith page's "Design decisions" (KV
+ * cache) fix it. Returns MK_EINVAL for a NULL model or a layer out of range. */
 int mk_kv_cache(mk_model* m, int layer, void** k_dev, void** v_dev);
 
 /* Copy the residual stream of the last step into out_dev (device fp32 [(n_layers+1)][hidden]):
- * row 0 = embedding output, row l+1 = residual after layer l. */
+ * row 0 = embedding output, row l+1 = residual after layer l. An addition of this library for
+ * per-layer parity checks (the pages have no counterpart). Synchronises the model's stream;
+ * MK_EINVAL for NULL arguments, MK_ECUDA if the copy fails. */
 int mk_debug_hidden(mk_model* m, float* out_dev);
 
-/* X-ray: copy the last step's trace (24-byte records: u64 globaltimer, u64 clock64, u32 smid,
- * u16 cta, u8 phase, u8 kind; one row of 2048 records per CTA, ended by a record of kind 255 where
- * it is not full) into host_buf. Returns MK_ENOTRACE without MK_FLAG_XRAY. */
+/* X-ray: copy the last step's trace into host_buf (the in-kernel timing of the monolith page,
+ * "Design decisions", "Timing": %globaltimer, clock64 and %smid stamped per block per phase; and
+ * its "M2: X-ray" milestone). Records are 24 bytes: u64 globaltimer, u64 clock64, u32 smid,
+ * u16 cta, u8 phase, u8 kind (0 phase begin, 1 phase end, 2 wait begin, 3 wait end, 4 sub-phase
+ * mark carrying only clock64); one row of 2048 records per CTA, ended by a record of kind 255
+ * where it is not full. host_buf must hold grid * 2048 * 24 bytes (MK_EINVAL otherwise);
+ * *written receives the bytes copied. Synchronises the model's stream. Returns MK_ENOTRACE if the
+ * model was created without MK_FLAG_XRAY. */
 int mk_trace_dump(mk_model* m, void* host_buf, size_t cap, size_t* written);
 
 /* Test hook: make CTA `cta` skip its signal after phase `phase` of layer 0 in the next steps, so
@@ -203,20 +214,27 @@ int mk_probe_cvt(uint32_t* f16_from_e4m3_dev, uint32_t* f16_from_e2m1_dev, const
 /* Largest max_ctx mk_decode_step_static accepts. */
 #define MK_STATIC_MAX_CTX 4352
 
-/* One decode step that allocates nothing, for callers that cannot allocate device memory when they
- * decode (code running during stream capture, hosts that own every device allocation, processes
- * that must not grow their device footprint after start-up). The pages have no counterpart: it is
- * mk_decode_step without a model object or workspace. The caller passes the weights (as for
- * mk_create), the bf16 KV cache as two device buffers k_dev, v_dev, each
- * [n_layers][n_kv_heads][cfg->max_ctx][head_dim], the token and position, and receives the next
- * token in *next_token_host (and the fp32 logits in logits_dev if not NULL).
+/* One decode step that allocates nothing. The pages have no counterpart: it is mk_decode_step
+ * without a model object or workspace, for callers that cannot allocate device memory at the
+ * moment they decode: a host framework that owns every device allocation and hands its plug-ins
+ * only fixed buffers, a process whose device footprint is fixed when it starts (a memory budget on
+ * a shared GPU), or a latency-critical loop that cannot afford cudaMalloc's implicit device-wide
+ * synchronisation. The caller passes the weights (as for mk_create, checked the same way), the
+ * bf16 KV cache as two device buffers k_dev, v_dev, each holding at least
+ * n_layers * n_kv_heads * cfg->max_ctx * head_dim elements laid out
+ * [n_layers][n_kv_heads][cfg->max_ctx][head_dim] (the library cannot check their size: a smaller
+ * buffer is read and written out of bounds), the token and position, and receives the next token
+ * in *next_token_host (and the fp32 logits in logits_dev if not NULL).
  * The kernel's scratch (sync words, activation exchange buffers, attention partials, layer table
  * and RoPE table, about 2.6 MB) lives in one fixed device array that every GPU loading the library
- * holds until the process exits; cfg->max_ctx <= MK_STATIC_MAX_CTX and n_layers <= 40.
- * The first call on a device looks the array up on that device (the device must be current), and
- * a call with a new rope_theta rebuilds its RoPE table. Calls share the array: two calls that run
- * at the same time on one GPU race and give wrong results. Synchronises `stream`. Errors:
- * MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, with text in mk_last_error(NULL). */
+ * holds until the process exits; cfg->max_ctx <= MK_STATIC_MAX_CTX and n_layers <= 40, larger
+ * values are rejected with MK_EINVAL. The first call on a device does a one-time set-up: it looks
+ * the array's device address up on that device (the device must be current) and checks the
+ * device as mk_create does; make that first call before any stream capture begins. A call with a
+ * new rope_theta rebuilds the RoPE table. Calls share the array, which keeps the last call's
+ * contents (the kernel clears the sync words it uses at the end of every step): two calls that
+ * overlap on one GPU race and give wrong results. Synchronises `stream` before it returns.
+ * Errors: MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, with text in mk_last_error(NULL). */
 int mk_decode_step_static(const mk_config* cfg, const mk_weights* w, void* k_dev, void* v_dev, int32_t token,
                           int32_t pos, int32_t* next_token_host, float* logits_dev, void* stream);
 

@@ -5,7 +5,7 @@
 // fp32 scale per output row, or NVFP4 (E2M1 codes, one E4M3 scale per 16 consecutive inputs,
 // one fp32 scale per tensor). Everything is computed in double precision, in the order the
 // definitions state; the only intermediate rounding is the bf16 KV cache, which is part of
-// the definition ("KV cache: stays bf16", monolith page, "Design decisions").
+// the definition (the KV cache is kept in bf16: monolith page, "Design decisions", KV cache).
 //
 // Only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline leg may load this library.
 // It shares no code, header, table or constant generator with the CUDA path.
@@ -18,7 +18,7 @@
 //   LM head = embedding matrix, argmax ................... monolith page, "Upstream facts" (Launch structure)
 //   bf16 KV cache ........................................ monolith page, "Design decisions" (KV cache)
 // Readings where the pages are silent (RoPE pairing, GQA mapping, eps, theta, scale formulas,
-// tie rules) are listed in the design doc and restated at each function below.
+// tie rules) are stated at each function below.
 
 #include <algorithm>
 #include <cmath>
@@ -307,8 +307,9 @@ double nvfp4_block(const uint16_t* p, uint8_t bc, float t, uint8_t* nib) {
   return err;
 }
 
-// NVFP4 with the per-block scale search the pages ask for ("round to nearest plus a per-block
-// scale search that minimizes MSE", monolith page, "Design decisions", NVFP4 format). Reading:
+// NVFP4 with the per-block scale search the pages ask for (round-to-nearest codes, and per block
+// the scale that gives the least squared error: monolith page, "Design decisions", NVFP4 format).
+// Reading:
 // the tensor scale is the amax one of quant_nvfp4; every E4M3 code 0 .. 0x7E (all non-negative
 // finite block scales) is a candidate; a candidate's E2M1 codes are round-to-nearest as in
 // quant_nvfp4 and its error is the summed squared reconstruction error of the block; the least

@@ -7,8 +7,7 @@
 #include <string>
 #include <vector>
 
-#include "../../include/mk.h"
-#include "mk_internal.h"
+#include "mk_host.h"
 
 using namespace mk;
 
@@ -119,6 +118,65 @@ static DMat to_dmat(const mk_mat& m) {
   return d;
 }
 
+// ------------------------------------------------------------------ checks shared by the entry points
+// (mk_create and mk_decode_step_static reject the same inputs with the same codes and messages)
+int mk::check_config(const mk_config* c, int max_layers) {
+  if (!c) return set_err(nullptr, MK_EINVAL, "config NULL");
+  if (c->hidden != HID || c->n_q_heads != NQH || c->n_kv_heads != NKVH || c->head_dim != HD || c->ffn != FFN)
+    return set_err(nullptr, MK_EINVAL, "only the Qwen3-0.6B shape family (1024/16/8/128/3072) is supported");
+  if (c->n_layers < 1 || c->n_layers > max_layers || c->vocab < 1 || c->vocab >= (1 << 24) || c->max_ctx < 1)
+    return set_err(nullptr, MK_EINVAL, "bad n_layers/vocab/max_ctx");
+  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return set_err(nullptr, MK_EINVAL, "bad eps/theta");
+  return MK_OK;
+}
+
+int mk::check_device(const mk_config* c, int* grid_out, int* max_units_out) {
+  int grid;
+  if (device_grid(&grid)) return set_err(nullptr, MK_ECUDA, "cannot query the device");
+  if (grid < 64) return set_err(nullptr, MK_ENORESIDENT, "need at least 64 SMs, device has %d", grid);
+  const int max_units = max_units_for(grid);
+  if (c->max_ctx > max_units * UNIT_POS)
+    return set_err(nullptr, MK_EINVAL, "max_ctx %d exceeds %d on this device", c->max_ctx, max_units * UNIT_POS);
+  int dev = 0, coop = 0, bps = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return set_err(nullptr, MK_ECUDA, "no current device");
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (!coop) return set_err(nullptr, MK_ENORESIDENT, "device lacks cooperative launch");
+  if (decode_occupancy(&bps) || bps < 1)
+    return set_err(nullptr, MK_ENORESIDENT, "persistent CTA (%d threads, %d B smem) does not fit an SM", NTHREADS,
+                   decode_smem_bytes());
+  *grid_out = grid;
+  *max_units_out = max_units;
+  return MK_OK;
+}
+
+int mk::check_weights(const mk_config* c, const mk_weights* w, DLayer* dl) {
+  if (!w || !w->layers) return set_err(nullptr, MK_EINVAL, "weights NULL");
+  int rc;
+  for (int l = 0; l < c->n_layers; ++l) {
+    const mk_layer& ly = w->layers[l];
+    const mk_mat* mats[7] = {&ly.q, &ly.k, &ly.v, &ly.o, &ly.gate, &ly.up, &ly.down};
+    const int rws[7] = {QROWS, KVROWS, KVROWS, HID, FFN, FFN, HID};
+    const int cls[7] = {HID, HID, HID, QROWS, HID, HID, FFN};
+    const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
+    for (int i = 0; i < 7; ++i) {
+      if ((rc = check_mat(*mats[i], rws[i], cls[i], names[i], true)) != MK_OK) return rc;
+      dl[l].m[i] = to_dmat(*mats[i]);
+    }
+    if (ly.q.fmt != ly.k.fmt || ly.q.fmt != ly.v.fmt)
+      return set_err(nullptr, MK_EINVAL, "layer %d: q, k, v must share one format", l);
+    if (ly.gate.fmt != ly.up.fmt) return set_err(nullptr, MK_EINVAL, "layer %d: gate and up must share one format", l);
+    if (!ly.ln_in || !ly.ln_post || !ly.q_norm || !ly.k_norm)
+      return set_err(nullptr, MK_EINVAL, "layer %d: norm weight NULL", l);
+    dl[l].ln_in = (const uint16_t*)ly.ln_in;
+    dl[l].ln_post = (const uint16_t*)ly.ln_post;
+    dl[l].q_norm = (const uint16_t*)ly.q_norm;
+    dl[l].k_norm = (const uint16_t*)ly.k_norm;
+  }
+  if ((rc = check_mat(w->embed, c->vocab, HID, "embed", false)) != MK_OK) return rc;
+  if (!w->final_norm) return set_err(nullptr, MK_EINVAL, "final_norm NULL");
+  return MK_OK;
+}
+
 extern "C" {
 
 int mk_decode_grid(void) {
@@ -146,54 +204,15 @@ int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes
               mk_model** out) {
   if (!out) return set_err(nullptr, MK_EINVAL, "out is NULL");
   *out = nullptr;
-  if (!c || !w || !w->layers) return set_err(nullptr, MK_EINVAL, "config or weights NULL");
-  if (c->hidden != HID || c->n_q_heads != NQH || c->n_kv_heads != NKVH || c->head_dim != HD || c->ffn != FFN)
-    return set_err(nullptr, MK_EINVAL, "only the Qwen3-0.6B shape family (1024/16/8/128/3072) is supported");
-  if (c->n_layers < 1 || c->n_layers > MAX_LAYERS || c->vocab < 1 || c->vocab >= (1 << 24) || c->max_ctx < 1)
-    return set_err(nullptr, MK_EINVAL, "bad n_layers/vocab/max_ctx");
-  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return set_err(nullptr, MK_EINVAL, "bad eps/theta");
-  int grid;
-  if (device_grid(&grid)) return set_err(nullptr, MK_ECUDA, "cannot query the device");
-  if (grid < 64) return set_err(nullptr, MK_ENORESIDENT, "need at least 64 SMs, device has %d", grid);
-  const int max_units = max_units_for(grid);
-  if (c->max_ctx > max_units * UNIT_POS)
-    return set_err(nullptr, MK_EINVAL, "max_ctx %d exceeds %d on this device", c->max_ctx, max_units * UNIT_POS);
-  int dev = 0, coop = 0, bps = 0;
-  cudaGetDevice(&dev);
-  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  if (!coop) return set_err(nullptr, MK_ENORESIDENT, "device lacks cooperative launch");
-  if (decode_occupancy(&bps) || bps < 1)
-    return set_err(nullptr, MK_ENORESIDENT, "persistent CTA (%d threads, %d B smem) does not fit an SM", NTHREADS,
-                   decode_smem_bytes());
+  int rc, grid, max_units;
+  if ((rc = check_config(c, MAX_LAYERS)) != MK_OK) return rc;
+  if ((rc = check_device(c, &grid, &max_units)) != MK_OK) return rc;
   Layout L = {};
   layout_of(c, flags, grid, &L);
   if (!ws || ws_bytes < L.total || !aligned16(ws))
     return set_err(nullptr, MK_EINVAL, "workspace too small or unaligned (%zu < %zu)", ws_bytes, L.total);
-  // weights
-  int rc;
   std::vector<DLayer> dl(c->n_layers);
-  for (int l = 0; l < c->n_layers; ++l) {
-    const mk_layer& ly = w->layers[l];
-    const mk_mat* mats[7] = {&ly.q, &ly.k, &ly.v, &ly.o, &ly.gate, &ly.up, &ly.down};
-    const int rws[7] = {QROWS, KVROWS, KVROWS, HID, FFN, FFN, HID};
-    const int cls[7] = {HID, HID, HID, QROWS, HID, HID, FFN};
-    const char* names[7] = {"q", "k", "v", "o", "gate", "up", "down"};
-    for (int i = 0; i < 7; ++i) {
-      if ((rc = check_mat(*mats[i], rws[i], cls[i], names[i], true)) != MK_OK) return rc;
-      dl[l].m[i] = to_dmat(*mats[i]);
-    }
-    if (ly.q.fmt != ly.k.fmt || ly.q.fmt != ly.v.fmt)
-      return set_err(nullptr, MK_EINVAL, "layer %d: q, k, v must share one format", l);
-    if (ly.gate.fmt != ly.up.fmt) return set_err(nullptr, MK_EINVAL, "layer %d: gate and up must share one format", l);
-    if (!ly.ln_in || !ly.ln_post || !ly.q_norm || !ly.k_norm)
-      return set_err(nullptr, MK_EINVAL, "layer %d: norm weight NULL", l);
-    dl[l].ln_in = (const uint16_t*)ly.ln_in;
-    dl[l].ln_post = (const uint16_t*)ly.ln_post;
-    dl[l].q_norm = (const uint16_t*)ly.q_norm;
-    dl[l].k_norm = (const uint16_t*)ly.k_norm;
-  }
-  if ((rc = check_mat(w->embed, c->vocab, HID, "embed", false)) != MK_OK) return rc;
-  if (!w->final_norm) return set_err(nullptr, MK_EINVAL, "final_norm NULL");
+  if ((rc = check_weights(c, w, dl.data())) != MK_OK) return rc;
 
   mk_model* m = new mk_model();
   m->cfg = *c;
@@ -304,8 +323,9 @@ static int collect_status(mk_model* m, int32_t* next_token) {
   }
   if (st != 0) {
     const uint32_t d = m->host_status[1];
-    set_err(m, MK_ETIMEOUT, "device wait timed out: phase %u layer %u cta %u%s", d & 0xFF, (d >> 8) & 0xFF,
-            (d >> 16) & 0x7FFF, (d & 0x80000000u) ? " (weight stream)" : "");
+    set_err(m, MK_ETIMEOUT, "device wait timed out: phase %u layer %u cta %u%s%s", d & 0xFF, (d >> 8) & 0xFF,
+            (d >> 16) & 0x7FFF, (d & 0x80000000u) ? " (weight stream)" : "",
+            m->host_status[3] ? "; a CTA exited with bulk copies still in flight" : "");
     cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
     cudaStreamSynchronize(m->stream);
     return MK_ETIMEOUT;

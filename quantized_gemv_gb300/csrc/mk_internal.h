@@ -55,7 +55,8 @@ struct SyncBlock {
   uint32_t c[8][32];           // per-phase arrival counters (reset by the last CTA of a step)
   uint32_t grp[NKVH][32];      // attention units finished, per KV head
   unsigned long long key[16];  // packed (logit, index) argmax key
-  uint32_t status[32];         // [0] status code, [1] detail word, [2] abort flag
+  uint32_t status[32];         // [0] status code, [1] detail word, [2] abort flag, [3] a CTA exited with
+                               // bulk copies still in flight (its drain gave up)
   int32_t tok[32];             // [0] token produced by the last step
 };
 

@@ -211,7 +211,15 @@ struct Producer {
         // consumers) and resumes it as soon as the slot is released
         while (!mbar_try_wait(&s->empty[slot], par)) {
           if (s->abort) return false;
-          if (globaltimer() - t0 > deadline_ns) return false;
+          if (globaltimer() - t0 > deadline_ns) {  // the consumers stopped releasing slots
+            if (P->sync) {
+              if (atomicCAS(&P->sync->status[0], 0u, 3u) == 0u)
+                st_relaxed_u32(&P->sync->status[1], (uint32_t)PH_WAIT | ((uint32_t)blockIdx.x << 16) | 0x80000000u);
+              st_relaxed_u32(&P->sync->status[2], 1u);
+            }
+            s->abort = 1;
+            return false;
+          }
         }
       }
     }
@@ -270,13 +278,19 @@ struct Producer {
     }
   }
   // Wait until every copy this producer issued has landed (used on abort, before the CTA exits).
+  // A copy still in flight after 200 ms is recorded in status word 3, so the host can report that
+  // the abandoned step did not end cleanly.
   __device__ void drain() {
     uint32_t first = n > NSLOT ? n - NSLOT : 0;
     for (uint32_t i = first; i < n; ++i) {
       uint32_t slot = i % NSLOT, par = (i / NSLOT) & 1;
       uint64_t t0 = globaltimer();
-      while (!mbar_test_wait(&s->full[slot], par))
-        if (globaltimer() - t0 > 200000000ull) break;
+      while (!mbar_test_wait(&s->full[slot], par)) {
+        if (globaltimer() - t0 > 200000000ull) {
+          if (P->sync) st_relaxed_u32(&P->sync->status[3], 1u);
+          return;
+        }
+      }
     }
   }
 };
@@ -1436,9 +1450,14 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_stream_read(const uint8_t* buf,
 // ------------------------------------------------------------------ launchers
 int decode_smem_bytes() { return SMEM_BYTES; }
 
-static bool g_attr_done = false;
+// Function attributes belong to the device that is current when they are set, so they are applied
+// once per device (a process that drives several GPUs sets them on each).
+constexpr int MAX_ATTR_DEVICES = 64;
+static bool g_attr_done[MAX_ATTR_DEVICES] = {};
 static int set_attrs() {
-  if (g_attr_done) return 0;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_ATTR_DEVICES) return -1;
+  if (g_attr_done[dev]) return 0;
   cudaError_t e;
   e = cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return -1;
@@ -1448,7 +1467,7 @@ static int set_attrs() {
   if (e != cudaSuccess) return -1;
   e = cudaFuncSetAttribute(k_stream_read, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return -1;
-  g_attr_done = true;
+  g_attr_done[dev] = true;
   return 0;
 }
 

@@ -1,24 +1,26 @@
 // mk_decode_step_static: one decode step that allocates nothing.
 //
-// Some callers cannot allocate device memory when they decode: code that runs while a CUDA stream
-// is being captured (cudaMalloc is not allowed there), code inside a host framework that owns every
-// device allocation and hands out only fixed buffers, or a process that must not grow its device
-// footprint after start-up. They still own the weights and the KV cache, but they cannot provide
-// the decode kernel's scratch (sync words, the tagged activation buffers, attention partials, the
-// layer table and the RoPE table). This file keeps that scratch in one file-scope __device__ array
-// of fixed size, so the step needs no workspace and no model object.
+// Some callers cannot allocate device memory at the moment they decode: a host framework that owns
+// every device allocation and hands its plug-ins only fixed buffers, a process that must not grow
+// its device footprint after start-up (a memory budget fixed when it was admitted to a shared GPU),
+// or a latency-critical loop where cudaMalloc's implicit device-wide synchronisation is not
+// acceptable. They still own the weights and the KV cache, but cannot provide the decode kernel's
+// scratch (sync words, the tagged activation buffers, attention partials, the layer table and the
+// RoPE table). This file keeps that scratch in one file-scope __device__ array of fixed size, so the
+// step needs no workspace and no model object.
 //
 // Limits and sharing: every GPU that loads the library holds the array until the process exits.
 // All calls on a device share it and it keeps the previous call's contents, so two calls that run
 // at the same time on one GPU (different streams, or different host threads without ordering)
 // race on it and give wrong results. The kernel resets the sync words it uses at the end of every
-// step; after a failed step they are cleared here.
+// step; after a failed step they are cleared here. The first call on a device looks the array's
+// device address up with that device current (cudaGetSymbolAddress); make that first call before
+// any stream capture begins. Every call synchronises the caller's stream before it returns.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
-#include "../../include/mk.h"
-#include "mk_internal.h"
+#include "mk_host.h"
 
 using namespace mk;
 
@@ -65,17 +67,17 @@ extern "C" {
 
 int mk_decode_step_static(const mk_config* c, const mk_weights* w, void* kv_k_dev, void* kv_v_dev, int32_t token,
                           int32_t pos, int32_t* next_token_host, float* logits_dev, void* stream) {
-  if (!c || !w || !w->layers || !kv_k_dev || !kv_v_dev || !next_token_host)
-    return fail(MK_EINVAL, "NULL argument");
-  if (c->hidden != HID || c->n_q_heads != NQH || c->n_kv_heads != NKVH || c->head_dim != HD || c->ffn != FFN)
-    return fail(MK_EINVAL, "only the Qwen3-0.6B shape family (1024/16/8/128/3072) is supported");
-  if (c->n_layers < 1 || c->n_layers > STATIC_MAX_LAYERS || c->vocab < 1 || c->vocab >= (1 << 24))
-    return fail(MK_EINVAL, "bad n_layers or vocab");
-  if (c->max_ctx < 1 || c->max_ctx > STATIC_MAX_CTX)
+  if (!c || !w || !kv_k_dev || !kv_v_dev || !next_token_host) return fail(MK_EINVAL, "NULL argument");
+  int rc;
+  if ((rc = check_config(c, STATIC_MAX_LAYERS)) != MK_OK) return rc;
+  if (c->max_ctx > STATIC_MAX_CTX)
     return fail(MK_EINVAL, "max_ctx must be at most MK_STATIC_MAX_CTX for the static entry point");
   if (token < 0 || token >= c->vocab || pos < 0 || pos >= c->max_ctx) return fail(MK_EINVAL, "token or pos out of range");
-  if (!(c->rms_eps > 0.f) || !(c->rope_theta > 0.f)) return fail(MK_EINVAL, "bad eps/theta");
   if (((uintptr_t)kv_k_dev & 15u) || ((uintptr_t)kv_v_dev & 15u)) return fail(MK_EINVAL, "KV cache not 16-byte aligned");
+  // the layer table of this call, checked like mk_create's (pageable source: the copy below
+  // completes before this call returns)
+  DLayer dl[STATIC_MAX_LAYERS];
+  if ((rc = check_weights(c, w, dl)) != MK_OK) return rc;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return fail(MK_ECUDA, "no current device");
   cudaStream_t st = (cudaStream_t)stream;
@@ -83,16 +85,13 @@ int mk_decode_step_static(const mk_config* c, const mk_weights* w, void* kv_k_de
   std::lock_guard<std::mutex> lock(g_mu);
   DevState& D = g_dev[dev];
   if (!D.ready) {  // set-up, once per device, with that device current
+    int grid = 0, mu = 0;
+    if ((rc = check_device(c, &grid, &mu)) != MK_OK) return rc;
     void* p = nullptr;
     cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return fail(MK_ECUDA, "cannot query the device");
-    int bps = 0;
-    if (sms < 64 || decode_occupancy(&bps) || bps < 1) return fail(MK_ENORESIDENT, "persistent grid does not fit");
     D.ptr = static_cast<StaticScratch*>(p);
-    D.grid = decode_grid_for(sms);
+    D.grid = grid;
     D.ready = true;
   }
   const int max_units = (D.grid / NKVH) > MAXC ? MAXC : (D.grid / NKVH);
@@ -104,32 +103,6 @@ int mk_decode_step_static(const mk_config* c, const mk_weights* w, void* kv_k_de
     if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
     D.rope_theta = c->rope_theta;
   }
-  // the layer table of this call (pageable source: the copy completes before this call returns it)
-  DLayer dl[STATIC_MAX_LAYERS];
-  for (int l = 0; l < c->n_layers; ++l) {
-    const mk_layer& ly = w->layers[l];
-    const mk_mat* mats[7] = {&ly.q, &ly.k, &ly.v, &ly.o, &ly.gate, &ly.up, &ly.down};
-    for (int i = 0; i < 7; ++i) {
-      const mk_mat& m = *mats[i];
-      if (m.fmt < MK_BF16 || m.fmt > MK_NVFP4 || !m.data || ((uintptr_t)m.data & 15u) ||
-          (m.fmt != MK_BF16 && (!m.scale || ((uintptr_t)m.scale & 15u))))
-        return fail(MK_EINVAL, "bad weight matrix");
-      dl[l].m[i].data = (const uint8_t*)m.data;
-      dl[l].m[i].scale = (const uint8_t*)m.scale;
-      dl[l].m[i].tscale = m.tensor_scale;
-      dl[l].m[i].fmt = m.fmt;
-    }
-    if (ly.q.fmt != ly.k.fmt || ly.q.fmt != ly.v.fmt || ly.gate.fmt != ly.up.fmt)
-      return fail(MK_EINVAL, "q/k/v and gate/up must share formats");
-    if (!ly.ln_in || !ly.ln_post || !ly.q_norm || !ly.k_norm) return fail(MK_EINVAL, "norm weight NULL");
-    dl[l].ln_in = (const uint16_t*)ly.ln_in;
-    dl[l].ln_post = (const uint16_t*)ly.ln_post;
-    dl[l].q_norm = (const uint16_t*)ly.q_norm;
-    dl[l].k_norm = (const uint16_t*)ly.k_norm;
-  }
-  if (w->embed.fmt != MK_BF16 && w->embed.fmt != MK_FP8_ROW) return fail(MK_EINVAL, "embedding must be bf16 or FP8");
-  if (!w->embed.data || (w->embed.fmt == MK_FP8_ROW && !w->embed.scale) || !w->final_norm)
-    return fail(MK_EINVAL, "embedding or final norm NULL");
   e = cudaMemcpyAsync(S->layers, dl, sizeof(DLayer) * c->n_layers, cudaMemcpyHostToDevice, st);
   if (e != cudaSuccess) return fail(MK_ECUDA, cudaGetErrorString(e));
 

@@ -106,8 +106,7 @@ def _ptr(t):
 
 def _check(rc, handle=None, what=""):
     if rc != MK_OK:
-        msg = lib().mk_last_error(handle).decode() if handle is not None or rc != MK_EINVAL else ""
-        raise MkError(rc, f"{what} {msg}".strip())
+        raise MkError(rc, f"{what} {lib().mk_last_error(handle).decode()}".strip())
 
 
 def _need_cuda(*ts):
@@ -304,8 +303,18 @@ MK_STATIC_MAX_CTX = 4352
 def decode_step_static(cfg: ModelConfig, packed, k_cache: torch.Tensor, v_cache: torch.Tensor, token: int,
                        pos: int, logits: torch.Tensor | None = None, stream=None) -> int:
     """mk_decode_step_static: one step with no model object and no workspace (the library keeps its
-    scratch in a fixed device array). k_cache / v_cache: bf16 CUDA tensors of
-    n_layers * n_kv_heads * max_ctx * head_dim elements (state the caller keeps between steps)."""
+    scratch in a fixed device array). k_cache / v_cache: contiguous bf16 CUDA tensors of at least
+    n_layers * n_kv_heads * max_ctx * head_dim elements (state the caller keeps between steps).
+    The library cannot see the caches' size, so it is checked here before the call."""
+    need = cfg.n_layers * cfg.n_kv_heads * cfg.max_ctx * cfg.head_dim
+    for name, t in (("k_cache", k_cache), ("v_cache", v_cache)):
+        if not (isinstance(t, torch.Tensor) and t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous()):
+            raise ValueError(f"{name} must be a contiguous bf16 CUDA tensor")
+        if t.numel() < need:
+            raise ValueError(f"{name} holds {t.numel()} elements, the model needs {need}")
+    if logits is not None and not (logits.is_cuda and logits.dtype == torch.float32 and logits.is_contiguous()
+                                   and logits.numel() >= cfg.vocab):
+        raise ValueError("logits must be a contiguous fp32 CUDA tensor of at least vocab elements")
     ccfg = mk_config(cfg.n_layers, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn, cfg.vocab,
                      cfg.max_ctx, cfg.rope_theta, cfg.rms_eps)
     layers = (mk_layer * cfg.n_layers)()

@@ -101,3 +101,19 @@ def test_invalid_arguments_are_rejected():
         with pytest.raises(mk.MkError) as ei:
             model.decode_step(tok, pos)
         assert ei.value.code == mk.MK_EINVAL
+
+
+def test_models_after_set_device_round_trip():
+    """Function attributes (the 232 KB shared-memory opt-in) are applied per device: models made
+    after switching the current device away and back, and on every visible device, still launch."""
+    cfg = S.ModelConfig(n_layers=1, vocab=1031, max_ctx=64)
+    master = S.master_weights(cfg, seed=83)
+    ref = None
+    for dev in list(range(torch.cuda.device_count())) + [0]:
+        torch.cuda.set_device(dev)
+        model = mk.Model(cfg, mk.pack_model(master, S.format_map("fp8"), device=f"cuda:{dev}"))
+        tok = model.decode_step(9, 0)
+        ref = tok if ref is None else ref
+        assert tok == ref
+        model.close()
+    torch.cuda.set_device(0)

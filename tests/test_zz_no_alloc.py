@@ -1,53 +1,85 @@
 """GPU: the allocation-free entry point (mk_decode_step_static) against the regular one.
 
-mk_decode_step_static is for callers that cannot allocate device memory when they decode (for
-example code running while a stream is captured, or a host framework that hands out only fixed
-buffers): its scratch lives in a fixed device array inside the library. It must give the same
-tokens and logits as mk_decode_step on the same weights, over consecutive calls that share that
-array. This file is collected last so that, if it fails, every other test has already run.
+mk_decode_step_static serves callers that cannot allocate device memory at the moment they
+decode: a host framework that owns every device allocation and hands out only fixed buffers, a
+process whose device footprint is fixed at start-up, or a loop that cannot afford cudaMalloc's
+implicit synchronisation. Its scratch lives in a fixed device array inside the library and keeps
+the previous call's contents. It runs the same kernel as mk_decode_step on the same inputs, so its
+tokens, logits and KV cache must be bit-identical to the regular step's, over consecutive calls
+that share that array, and across a change of rope_theta (which rebuilds the RoPE table). This
+file is collected last so that, if it fails, every other test has already run.
 """
-import numpy as np
+import dataclasses
+
 import pytest
 import torch
 
 from quantized_gemv_gb300 import mk
 from quantized_gemv_gb300 import synthetic as S
-from tests.gpu_util import LOGIT_ATOL
 
 pytestmark = pytest.mark.gpu
+
+
+def _caches(cfg):
+    n = cfg.n_layers * cfg.n_kv_heads * cfg.max_ctx * cfg.head_dim
+    return (torch.zeros(n, dtype=torch.bfloat16, device="cuda"), torch.zeros(n, dtype=torch.bfloat16, device="cuda"))
+
+
+def _run_pair(cfg, packed, k_cache, v_cache, tokens):
+    """Steps at positions 0.. on both entry points (teacher-forced on `tokens`); asserts bit-equal
+    tokens and logits at every step."""
+    model = mk.Model(cfg, packed)
+    for pos, tok in enumerate(tokens):
+        la = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+        lb = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+        na = model.decode_step(tok, pos, la)
+        nb = mk.decode_step_static(cfg, packed, k_cache, v_cache, tok, pos, lb)
+        assert na == nb, (pos, na, nb)
+        assert torch.equal(la.view(torch.int32), lb.view(torch.int32)), pos
+    n = len(tokens)
+    for l in range(cfg.n_layers):
+        kt, vt = model.kv_cache(l)
+        ks = k_cache.view(cfg.n_layers, cfg.n_kv_heads, cfg.max_ctx, cfg.head_dim)[l]
+        vs = v_cache.view(cfg.n_layers, cfg.n_kv_heads, cfg.max_ctx, cfg.head_dim)[l]
+        assert torch.equal(kt[:, :n].view(torch.int16), ks[:, :n].view(torch.int16))
+        assert torch.equal(vt[:, :n].view(torch.int16), vs[:, :n].view(torch.int16))
+    model.close()
 
 
 @pytest.mark.parametrize("variant", ["fp8", "bf16"])
 def test_static_step_matches_regular_step(variant):
     cfg = S.ModelConfig(n_layers=2, vocab=4099, max_ctx=256)
     packed = mk.pack_model(S.master_weights(cfg, seed=91), S.format_map(variant))
-    model = mk.Model(cfg, packed)
-    n = cfg.n_layers * cfg.n_kv_heads * cfg.max_ctx * cfg.head_dim
-    k_cache = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
-    v_cache = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
-    tok = 17
-    for pos in range(4):  # consecutive calls: the shared scratch carries over between them
-        la = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
-        lb = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
-        na = model.decode_step(tok, pos, la)
-        nb = mk.decode_step_static(cfg, packed, k_cache, v_cache, tok, pos, lb)
-        assert na == nb
-        assert float(np.max(np.abs(la.cpu().numpy() - lb.cpu().numpy()))) <= LOGIT_ATOL
-        tok = na
-    # the caller's cache holds what the model's own cache holds
-    for l in range(cfg.n_layers):
-        kt, vt = model.kv_cache(l)
-        ks = k_cache.view(cfg.n_layers, cfg.n_kv_heads, cfg.max_ctx, cfg.head_dim)[l]
-        vs = v_cache.view(cfg.n_layers, cfg.n_kv_heads, cfg.max_ctx, cfg.head_dim)[l]
-        assert torch.equal(kt[:, :4], ks[:, :4]) and torch.equal(vt[:, :4], vs[:, :4])
-    model.close()
+    k_cache, v_cache = _caches(cfg)
+    # two calls in a row on one array, then more: the scratch carries over between them
+    _run_pair(cfg, packed, k_cache, v_cache, [17, 4000, 3, 1234])
+
+
+def test_static_step_follows_rope_theta():
+    """A second theta rebuilds the static RoPE table, and going back to the first rebuilds it again."""
+    cfg_a = S.ModelConfig(n_layers=1, vocab=1031, max_ctx=128)
+    cfg_b = dataclasses.replace(cfg_a, rope_theta=1e4)
+    packed = mk.pack_model(S.master_weights(cfg_a, seed=93), S.format_map("fp8"))
+    for cfg in (cfg_a, cfg_b, cfg_a):
+        k_cache, v_cache = _caches(cfg)
+        _run_pair(cfg, packed, k_cache, v_cache, [5, 77, 901])
 
 
 def test_static_step_rejects_oversized_context():
     cfg = S.ModelConfig(n_layers=1, vocab=64, max_ctx=mk.MK_STATIC_MAX_CTX + 64)
     packed = mk.pack_model(S.master_weights(cfg, seed=92), S.format_map("bf16"))
-    n = cfg.n_layers * cfg.n_kv_heads * cfg.max_ctx * cfg.head_dim
-    kc = torch.zeros(n, dtype=torch.bfloat16, device="cuda")
+    kc, vc = _caches(cfg)
     with pytest.raises(mk.MkError) as ei:
-        mk.decode_step_static(cfg, packed, kc, kc, 1, 0)
+        mk.decode_step_static(cfg, packed, kc, vc, 1, 0)
     assert ei.value.code == mk.MK_EINVAL
+    assert "MK_STATIC_MAX_CTX" in str(ei.value)
+
+
+def test_static_step_rejects_small_cache():
+    cfg = S.ModelConfig(n_layers=1, vocab=64, max_ctx=64)
+    packed = mk.pack_model(S.master_weights(cfg, seed=94), S.format_map("bf16"))
+    kc, vc = _caches(cfg)
+    with pytest.raises(ValueError):
+        mk.decode_step_static(cfg, packed, kc[:-1], vc, 1, 0)
+    with pytest.raises(ValueError):
+        mk.decode_step_static(cfg, packed, kc, vc.float(), 1, 0)
