@@ -7,20 +7,25 @@ A "step" is one decode step: one launch of the decode kernel producing one token
 P..P+K-1 after the workload's 32-token prompt or prefilled KV), launched back to back with the
 input token of each launch read from device memory; it is bracketed by a barrier and
 torch.cuda.synchronize() and timed with CUDA events on the launching stream. Warm-up runs the
-same positions W times first. Every step streams >= 0.4 GB of weights, far above the 135 MB L2,
+same positions W times first. Every step streams >= 0.4 GB of weights, more than the L2 holds,
 so no L2 flush is needed between steps.
 
 Extra keys beyond the base contract: `roofline` (the decode kernel against the measured HBM copy
-bandwidth), `cpu_baseline` (the CPU oracle on this host's cores, a bounded sample), `e2e` (the
-same metric through mk_decode_step, which returns each token to the host), `clocks` (NVML samples
-during the timed region), `stream_read_gbs` (the library's bulk-copy streaming-read probe, same
-run) and `variants` (the FP8, NVFP4 (amax and searched block scales; all-NVFP4), bf16-head FP8,
-bf16-scale FP8 and long-context FP8 workloads, each timed the same way).
+bandwidth), `runs` (five more timed regions of the same K steps: median, min and max, the pages'
+benchmark protocol), `cpu_baseline` (the CPU oracle on this host's cores in a fresh process, a
+bounded sample, with a one-thread figure), `e2e` (the same metric through mk_decode_step, which
+returns each token to the host), `clocks` (NVML samples during the timed region),
+`stream_read_gbs` (the library's bulk-copy streaming-read probe, same run), `variants` (the FP8,
+NVFP4 (amax and searched block scales; all-NVFP4), bf16-head FP8, bf16-scale FP8 and long-context
+FP8 workloads, each timed the same way), `xray` (the instrumented build's split of a token, its
+overhead and its span against the launch time, for the headline and the long-context workload),
+`layer1_bf16` (one layer + the LM head, timed cold after an L2 scrub and warm) and `sweep`
+(throughput and energy against context length, FP8).
 
 --impl reference times the CPU oracle (the only reference implementation of this method) on the
-same workload and prints its line with "impl": "reference". Under torchrun, rank 0 alone runs it.
-Multi-GPU: each rank decodes its own independent replica (the path has no data-parallel
-exchange); value = tokens of all ranks / the slowest rank's time.
+same workload and positions and prints its line with "impl": "reference". Under torchrun, rank 0
+alone runs it. Multi-GPU: each rank decodes its own independent replica (the path has no
+data-parallel exchange); value = tokens of all ranks / the slowest rank's time.
 """
 from __future__ import annotations
 
@@ -43,8 +48,8 @@ sys.path.insert(0, ROOT)
 from quantized_gemv_gb300 import synthetic as S  # noqa: E402
 
 HEADLINE = "qwen3_0.6b_bf16"
-UPSTREAM_BF16_TOKS = 1033.0
-NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (about 8 TB/s); the roofline divides by the measured copy  # RTX 5090 upstream kernel, bf16 (monolith page, "Upstream facts")
+UPSTREAM_BF16_TOKS = 1033.0  # RTX 5090 upstream kernel, bf16 (monolith page, "Upstream facts")
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (about 8 TB/s); the roofline divides by the measured copy
 
 
 # ------------------------------------------------------------------ byte accounting
@@ -171,11 +176,12 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ GPU arm
-def setup_model(wl: S.Workload, mk):
+def setup_model(wl: S.Workload, mk, flags: int = 0, master=None):
     cfg = wl.config()
-    master = S.master_weights(cfg, seed=0)
+    if master is None:
+        master = S.master_weights(cfg, seed=0)
     packed = mk.pack_model(master, S.format_map(wl.variant))
-    model = mk.Model(cfg, packed)
+    model = mk.Model(cfg, packed, flags=flags)
     start_pos = 0
     if wl.prefill:
         k, v = S.prefill_kv(cfg, wl.prefill, seed=2)
@@ -262,31 +268,34 @@ def stream_read_gbs(mk):
 
 
 def oracle_sample(wl: S.Workload, master, seconds: float = 12.0, steps: int | None = None, warmup: int = 0,
-                  budget_s: float = 150.0):
+                  budget_s: float = 150.0, threads: int | None = None):
     """The CPU oracle decoding the same workload on this host's cores, at the positions the GPU arm
     times: the prompt (or the prefilled KV cache) first, untimed, then `warmup` untimed greedy
-    steps, then timed greedy steps: `steps` of them, or as many as fit in `seconds` when steps is
-    None, and never more than fit in `budget_s` (the sample says how many were timed)."""
+    steps from the first timed position, then timed greedy steps from that same position again
+    (they rewrite the same cache rows with the same values): `steps` of them, or as many as fit in
+    `seconds` when steps is None, and never more than fit in `budget_s` (the sample says how many
+    were timed). `threads`: oracle threads (default: every core this process may use)."""
     from oracle import oracle as O
     cfg = wl.config()
-    cores = len(os.sched_getaffinity(0))
-    packed = O.pack_model(master, S.format_map(wl.variant), cores)
+    cores = len(os.sched_getaffinity(0)) if threads is None else int(threads)
+    packed = O.pack_model(master, S.format_map(wl.variant), len(os.sched_getaffinity(0)))
     om = O.OracleModel(cfg, packed, n_threads=cores)
     if wl.prefill:
         k, v = S.prefill_kv(cfg, wl.prefill, seed=2)
         om.set_kv(k, v)
-        pos, tok = wl.prefill, int(S.prompt_ids(cfg, 1)[0])
+        pos0, tok0 = wl.prefill, int(S.prompt_ids(cfg, 1)[0])
     else:
         prompt = S.prompt_ids(cfg, wl.prompt_len)
         tok = int(prompt[0])
         for pos in range(wl.prompt_len):
             nxt, _, _, _ = om.step(tok, pos, want_logits=False)
             tok = int(prompt[pos + 1]) if pos + 1 < wl.prompt_len else nxt
-        pos = wl.prompt_len
+        pos0, tok0 = wl.prompt_len, tok
+    tok, pos = tok0, pos0
     for _ in range(max(warmup, 0)):
         tok, _, _, _ = om.step(tok, pos, want_logits=False)
         pos += 1
-    first, n, t0 = pos, 0, time.perf_counter()
+    tok, pos, n, t0 = tok0, pos0, 0, time.perf_counter()
     while True:
         tok, _, _, _ = om.step(tok, pos, want_logits=False)
         pos += 1
@@ -299,36 +308,58 @@ def oracle_sample(wl: S.Workload, master, seconds: float = 12.0, steps: int | No
         if el >= budget_s and n >= 2:
             break
     return {"value": n / el, "unit": "tok/s", "cores": cores, "kind": "oracle", "steps": n,
-            "sample": f"{n} timed greedy steps of {wl.name} at positions {first}..{pos - 1} after "
-                      f"{'the prefilled KV' if wl.prefill else 'the prompt'} and {max(warmup, 0)} untimed steps "
-                      f"({el:.1f} s, double precision, {cores} threads)"}
+            "positions": f"{pos0}..{pos - 1}",
+            "sample": f"{n} timed greedy steps of {wl.name} at positions {pos0}..{pos - 1} after "
+                      f"{'the prefilled KV' if wl.prefill else 'the prompt'} and {max(warmup, 0)} untimed steps at "
+                      f"the same positions ({el:.1f} s, double precision, {cores} threads)"}
 
 
-def xray_summary(wl: S.Workload, mk, master, steps: int = 16):
+def cpu_leg_subprocess(wl: S.Workload, seconds: float, one_thread_seconds: float):
+    """The oracle timed in a fresh process (no CUDA context or torch thread pool competing with its
+    threads): all cores, then one thread. Returns the all-core sample with the one-thread figure."""
+    import subprocess
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-leg", "--workload", wl.name,
+           "--cpu-seconds", str(seconds), "--cpu-seconds-1t", str(one_thread_seconds)]
+    env = dict(os.environ, OMP_NUM_THREADS="1", CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=900)
+    if r.returncode != 0:
+        return {"value": None, "unit": "tok/s", "kind": "oracle", "error": r.stderr[-400:]}
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
+def run_cpu_leg(wl: S.Workload, seconds: float, one_thread_seconds: float):
+    master = S.master_weights(wl.config(), seed=0)
+    allc = oracle_sample(wl, master, seconds=seconds)
+    one = oracle_sample(wl, master, seconds=one_thread_seconds, threads=1)
+    allc["one_thread"] = {"value": one["value"], "steps": one["steps"], "sample": one["sample"]}
+    allc["process"] = "a fresh process (no CUDA context), OMP_NUM_THREADS=1 for torch"
+    print(json.dumps(allc))
+
+
+def xray_summary(wl: S.Workload, mk, master, steps: int = 16, plain_tok_s: float | None = None):
     """The same workload through the instrumented build (MK_FLAG_XRAY): the last step's split of a
-    token into weight-read, wait, attention and LM-head time, and the instrumented throughput."""
+    token into weight-read, wait, attention and LM-head time, the instrumented throughput against
+    the plain one, and the X-ray's own span of the last step against that launch's CUDA-event time
+    (the two checks of the X-ray milestone: overhead within 3 %, summed phases within 5 %)."""
     from quantized_gemv_gb300 import xray
-    cfg = wl.config()
-    packed = mk.pack_model(master, S.format_map(wl.variant))
-    model = mk.Model(cfg, packed, flags=mk.MK_FLAG_XRAY)
-    prompt = S.prompt_ids(cfg, wl.prompt_len)
-    tok = int(prompt[0])
-    for pos in range(wl.prompt_len):
-        nxt = model.decode_step(tok, pos)
-        tok = int(prompt[pos + 1]) if pos + 1 < wl.prompt_len else nxt
-    total_ms, _, _ = time_steps(model, tok, wl.prompt_len, steps, 2)
+    cfg, _, model, pos0, first = setup_model(wl, mk, flags=mk.MK_FLAG_XRAY, master=master)
+    total_ms, per, _ = time_steps(model, first, pos0, steps, 3)
     tr = model.trace()
     a = xray.analyze(tr)
     cp = xray.critical_path(tr)
     model.close()
     t = a["token_ns"]
+    inst = steps / (total_ms * 1e-3)
     return {"token_us": round(t / 1e3, 1), "ctas": a["ctas"],
             "weight_read_share": round(a["weight_read_ns"] / t, 3), "barrier_wait_share": round(a["barrier_wait_share"], 3),
             "attention_share": round(a["attention_ns"] / t, 3), "lm_head_share": round(a["lm_head_ns"] / t, 3),
-            "instrumented_tok_s": round(steps / (total_ms * 1e-3), 1),
+            "instrumented_tok_s": round(inst, 1),
+            "overhead_vs_plain": round(plain_tok_s / inst - 1.0, 4) if plain_tok_s else None,
+            "last_launch_us": round(per[-1] * 1e3, 1),
+            "span_over_launch": round(t / 1e3 / (per[-1] * 1e3), 4),
             "critical_path_us": {k: round(v / 1e3, 3) for k, v in cp.items() if k != "layers"},
-            "note": "one instrumented step at the end of a 16-step greedy run; shares of the token's wall time, "
-                    "averaged over CTAs"}
+            "note": f"the last of {steps} instrumented steps from position {pos0}; shares of the token's wall "
+                    "time, averaged over CTAs; span_over_launch = first-to-last stamp / CUDA-event launch time"}
 
 
 SWEEP_POSITIONS = (16, 128, 512, 1024, 2048)
@@ -368,7 +399,10 @@ def run_sweep(mk, steps: int = 32, warmup: int = 3):
             "data": "synthetic (seeded N(0,0.02) weights; KV cache prefilled N(0,1) bf16)", "sweep": rows}
 
 
-def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_steps: int | None = None):
+def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_steps: int | None = None,
+                 runs: int = 5):
+    """The contract's timed region of `steps` launches, then `runs` more regions of the same
+    positions for the median / min / max the pages' benchmark protocol reports."""
     cfg, master, model, pos0, first = setup_model(wl, mk)
     k = steps
     if pos0 + k > cfg.max_ctx:
@@ -376,6 +410,10 @@ def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_ste
     sampler = ClockSampler(torch.cuda.current_device())
     with sampler:
         total_ms, per, toks = time_steps(model, first, pos0, k, warmup, dist)
+        rates = []
+        for _ in range(runs):
+            t_ms, _, _ = time_steps(model, first, pos0, k, 0)
+            rates.append(k / (t_ms * 1e-3))
     e2e_ms = time_e2e(model, first, pos0, e2e_steps or k)
     wbytes = weight_bytes(cfg, wl.variant)
     mean_pos = pos0 + (k - 1) / 2
@@ -383,11 +421,51 @@ def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_ste
     res = {"tok_s": k / (total_ms * 1e-3), "ms_per_step": total_ms / k, "launch_ms": launch_ms,
            "weight_bytes": wbytes, "kv_bytes": kv_bytes(cfg, int(round(mean_pos))),
            "e2e_tok_s": (e2e_steps or k) / (e2e_ms * 1e-3), "clocks": sampler.summary(),
-           "watts": sampler.watts(), "first_tokens": toks[:4].tolist()}
+           "watts": sampler.watts(), "first_tokens": toks[:4].tolist(),
+           "runs": {"n": runs, "steps_each": k, "median_tok_s": round(statistics.median(rates), 1),
+                    "min_tok_s": round(min(rates), 1), "max_tok_s": round(max(rates), 1)} if runs else None}
     res["weight_gbs"] = wbytes / (launch_ms * 1e-3) / 1e9
     res["total_gbs"] = (wbytes + res["kv_bytes"]) / (launch_ms * 1e-3) / 1e9
     model.close()
     return res, master
+
+
+def run_layer1(mk, repeats: int = 21):
+    """One bf16 decoder layer + the tied 151,936-row LM head, KV prefilled with 16 positions, one step
+    at position 16: its 342.7 MB fit the 126 MB L2 only in part, so it is timed both after a 512 MB
+    scrub of L2 before every repeat (cold) and back to back (warm). Each repeat is one launch timed
+    with CUDA events; median, min and max over the repeats."""
+    wl = S.WORKLOADS["layer1_bf16"]
+    cfg, _, model, pos0, first = setup_model(wl, mk)
+    tok = torch.tensor([first], dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(1, dtype=torch.int32, device="cuda")
+    scrub = torch.empty(512 << 20, dtype=torch.uint8, device="cuda")
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    stream = model.stream
+    out = {}
+    for mode in ("cold", "warm"):
+        ms = []
+        for i in range(repeats + 3):
+            if mode == "cold":
+                scrub.fill_(i & 0xFF)
+            torch.cuda.synchronize()
+            with torch.cuda.stream(stream):
+                e0.record(stream)
+                model.decode_next(tok, pos0, nxt)
+                e1.record(stream)
+            torch.cuda.synchronize()
+            if i >= 3:
+                ms.append(e0.elapsed_time(e1))
+        model.sync()
+        med = statistics.median(ms)
+        b = weight_bytes(cfg, wl.variant) + kv_bytes(cfg, pos0)
+        out[mode] = {"median_ms": round(med, 5), "min_ms": round(min(ms), 5), "max_ms": round(max(ms), 5),
+                     "tok_s": round(1e3 / med, 1), "gbs": round(b / (med * 1e-3) / 1e9, 1)}
+    del scrub
+    model.close()
+    out["bytes_per_step"] = weight_bytes(cfg, wl.variant) + kv_bytes(cfg, pos0)
+    out["l2"] = "cold: a 512 MB buffer written before every repeat; warm: repeats back to back"
+    return out
 
 
 def whole_job_rate(local_total_ms: float, steps: int, world: int, dist=None):
@@ -413,9 +491,17 @@ def main():
     ap.add_argument("--no-variants", action="store_true", help="skip the FP8/NVFP4/long-context lines")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-xray", action="store_true", help="skip the instrumented-build summary")
-    ap.add_argument("--sweep", action="store_true", help="print the context-length sweep (FP8) instead")
+    ap.add_argument("--sweep", action="store_true", help="print the context-length sweep (FP8) alone")
+    ap.add_argument("--no-sweep", action="store_true", help="leave the context-length sweep out of the line")
+    ap.add_argument("--no-layer1", action="store_true", help="leave the one-layer workload out of the line")
+    ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)  # internal: the oracle leg
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
+    ap.add_argument("--cpu-seconds-1t", type=float, default=10.0, help=argparse.SUPPRESS)
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.cpu_leg:  # runs in a fresh process started by the GPU arm
+        run_cpu_leg(S.WORKLOADS[args.workload], args.cpu_seconds, args.cpu_seconds_1t)
+        return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -431,6 +517,7 @@ def main():
         if rank != 0:
             return
         master = S.master_weights(wl.config(), seed=0)
+        # warm-up steps replay the first timed positions, so the timed positions are the GPU arm's
         cb = oracle_sample(wl, master, steps=args.steps, warmup=args.warmup)
         line = {"metric": "batch-1 decode tok/s (Qwen3-0.6B shape)", "value": cb["value"], "unit": "tok/s",
                 "impl": "reference", "device": "host cpu", "n_gpus": args.gpus, "steps": cb["steps"],
@@ -462,6 +549,7 @@ def main():
             w2 = S.WORKLOADS[name]
             r2, _ = run_workload(w2, min(args.steps, w2.steps), args.warmup, mk, None, e2e_steps=16)
             variants[name] = {"tok_s": round(r2["tok_s"], 1), "ms_per_step": round(r2["ms_per_step"], 4),
+                              "runs": r2["runs"],
                               "watts": round(r2["watts"], 1) if r2["watts"] else None,
                               "weight_gbs": round(r2["weight_gbs"], 1),
                               "roofline_frac_weights": round(r2["weight_gbs"] / peak, 4),
@@ -469,11 +557,19 @@ def main():
                               "frac_of_nominal_weights_kv": round(r2["total_gbs"] / NOMINAL_HBM_GBS, 4),
                               "e2e_tok_s": round(r2["e2e_tok_s"], 1), "clocks": r2["clocks"]}
     xr = None
-    if rank == 0 and not args.no_xray and not wl.prefill:
-        xr = xray_summary(wl, mk, master)
+    if rank == 0 and not args.no_xray:
+        xr = xray_summary(wl, mk, master, plain_tok_s=res["runs"]["median_tok_s"])
+        if not args.no_variants and wl.name != "qwen3_0.6b_fp8_ctx4096":
+            v = variants.get("qwen3_0.6b_fp8_ctx4096")
+            xr_ctx = xray_summary(S.WORKLOADS["qwen3_0.6b_fp8_ctx4096"], mk, None,
+                                  plain_tok_s=v["runs"]["median_tok_s"] if v else None)
+            xr = {"headline": xr, "qwen3_0.6b_fp8_ctx4096": xr_ctx}
+    layer1 = run_layer1(mk) if rank == 0 and not args.no_layer1 else None
+    sweep = run_sweep(mk) if rank == 0 and not args.no_sweep else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        cpu = oracle_sample(wl, master, seconds=12.0)
+        del master
+        cpu = cpu_leg_subprocess(wl, 12.0, 10.0)
     if rank != 0:
         return
     line = {
@@ -487,7 +583,7 @@ def main():
                    "global_batch": world, "positions": f"{S.WORKLOADS[wl.name].prompt_len + wl.prefill}.."
                    f"{S.WORKLOADS[wl.name].prompt_len + wl.prefill + args.steps - 1}",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "no flush: every step reads >= 0.4 GB of weights, L2 is 135 MB"},
+                   "l2": "no flush: every step reads >= 0.4 GB of weights, more than the 126 MB L2"},
         "weight_stream_gbs": round(res["weight_gbs"], 1),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": profiled_traffic(wl.name),
@@ -505,8 +601,11 @@ def main():
         "energy": {"watts": round(res["watts"], 1) if res["watts"] else None,
                    "tok_per_joule": round(value / world / res["watts"], 2) if res["watts"] else None,
                    "source": "NVML board power, median over the timed region"},
+        "runs": res["runs"],
         "xray": xr,
         "variants": variants,
+        "layer1_bf16": layer1,
+        "sweep": sweep["sweep"] if sweep else None,
     }
     print(json.dumps(line))
 

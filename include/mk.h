@@ -81,6 +81,17 @@ typedef struct mk_model mk_model; /* opaque; library-owned host object */
 
 /* mk_create flags */
 #define MK_FLAG_XRAY 1u /* keep per-CTA per-phase timestamps of the last step (mk_trace_dump) */
+/* MK_FLAG_XRAY plus sub-phase marks inside each phase (kind 4 records, SM clock only): a finer
+ * split of a phase at a higher cost (the marks slow a token by several per cent). */
+#define MK_FLAG_XRAY_MARKS 4u
+/* Keep the o_proj GEMV step at every context length. By default, on a decode grid of 128 CTAs
+ * and where every layer's W_o has one format, steps whose context fits one attention unit
+ * (pos < 288) fold the O-projection into attention: every CTA attends for one q head and
+ * multiplies the output by its 128 x 128 block of W_o (repacked into the workspace by mk_create),
+ * and the 16 heads' partial sums meet in order-independent integer accumulators, which removes
+ * one step and one exchange a layer. The results equal the unfolded step's within fp32 rounding
+ * and are deterministic. */
+#define MK_FLAG_NO_FOLD 8u
 
 /* ---------------------------------------------------------------- model lifetime */
 

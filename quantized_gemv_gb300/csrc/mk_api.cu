@@ -27,6 +27,10 @@ struct mk_model {
   uint16_t *kc, *vc;
   float* hidden_dbg;
   TraceRec* trace;
+  bool fold_o;                 // W_o repacked for the folded O-projection (used at short contexts)
+  uint8_t* wo_rep;
+  size_t wo_lbytes;
+  unsigned long long* acc;     // count words, two sets of [n_layers][HID] (launch parity)
   DMat embed;
   const uint16_t* final_norm;
   // host
@@ -54,7 +58,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 void mk::set_global_error(const char* msg) { g_create_err = msg; }
 
 struct Layout {
-  size_t sync, layers, h_mlp, h_attn, qkv, att, act, attp, rope_cos, rope_sin, kc, vc, hidden, trace, total;
+  size_t sync, layers, h_mlp, h_attn, qkv, att, act, attp, rope_cos, rope_sin, kc, vc, hidden, trace, acc, wo, total;
 };
 
 static int device_grid(int* grid) {
@@ -90,9 +94,14 @@ static bool layout_of(const mk_config* c, unsigned flags, int grid, Layout* L) {
   L->rope_cos = take((size_t)c->max_ctx * (HD / 2) * 4);
   L->rope_sin = take((size_t)c->max_ctx * (HD / 2) * 4);
   L->hidden = take((size_t)(c->n_layers + 1) * HID * 4);
-  L->trace = take((flags & MK_FLAG_XRAY) ? (size_t)grid * TRACE_PER_CTA * sizeof(TraceRec) : 0);
+  L->trace = take((flags & (MK_FLAG_XRAY | MK_FLAG_XRAY_MARKS)) ? (size_t)grid * TRACE_PER_CTA * sizeof(TraceRec) : 0);
   L->kc = take(kv);
   L->vc = take(kv);
+  // folded O-projection: count words (two sets) and W_o repacked per (head, slice) block, sized
+  // for bf16, the widest format
+  const bool fold = !(flags & MK_FLAG_NO_FOLD) && grid == FOLD_GRID;
+  L->acc = take(fold ? 2 * (size_t)c->n_layers * HID * sizeof(unsigned long long) : 0);
+  L->wo = take(fold ? (size_t)c->n_layers * NQH * FOLD_SLICES * wo_block_bytes(0) : 0);
   L->total = o;
   return true;
 }
@@ -235,9 +244,15 @@ int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes
   m->kc = (uint16_t*)(base + L.kc);
   m->vc = (uint16_t*)(base + L.vc);
   m->hidden_dbg = (float*)(base + L.hidden);
-  m->trace = (flags & MK_FLAG_XRAY) ? (TraceRec*)(base + L.trace) : nullptr;
+  m->trace = (flags & (MK_FLAG_XRAY | MK_FLAG_XRAY_MARKS)) ? (TraceRec*)(base + L.trace) : nullptr;
   m->embed = to_dmat(w->embed);
   m->final_norm = (const uint16_t*)w->final_norm;
+  // the folded O-projection needs the grid of 128 and one W_o format in every layer
+  m->fold_o = !(flags & MK_FLAG_NO_FOLD) && grid == FOLD_GRID;
+  for (int l = 1; m->fold_o && l < c->n_layers; ++l) m->fold_o = w->layers[l].o.fmt == w->layers[0].o.fmt;
+  m->acc = m->fold_o ? (unsigned long long*)(base + L.acc) : nullptr;
+  m->wo_rep = m->fold_o ? base + L.wo : nullptr;
+  m->wo_lbytes = m->fold_o ? (size_t)NQH * FOLD_SLICES * wo_block_bytes(w->layers[0].o.fmt) : 0;
   m->timeout_ns = 500000000ull;
   m->fault_cta = -1;
   m->fault_phase = -1;
@@ -250,6 +265,10 @@ int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes
     e = cudaMemcpyAsync(m->dlayers, dl.data(), sizeof(DLayer) * c->n_layers, cudaMemcpyHostToDevice, m->stream);
   if (e == cudaSuccess && launch_rope_table(m->rope_cos, m->rope_sin, c->max_ctx, c->rope_theta, m->stream))
     e = cudaGetLastError();
+  for (int l = 0; m->fold_o && e == cudaSuccess && l < c->n_layers; ++l)
+    if (launch_repack_o(w->layers[l].o.data, w->layers[l].o.scale, w->layers[l].o.fmt, m->wo_rep + l * m->wo_lbytes,
+                        m->stream))
+      e = cudaGetLastError();
   if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
   if (e != cudaSuccess) {
     set_err(nullptr, MK_ECUDA, "mk_create: %s", cudaGetErrorString(e));
@@ -301,10 +320,24 @@ static KParams base_params(mk_model* m) {
   return p;
 }
 
+// X-ray level of the model's launches (see launch_decode).
+static int xray_level(const mk_model* m) {
+  return m->trace == nullptr ? 0 : ((m->flags & MK_FLAG_XRAY_MARKS) ? 2 : 1);
+}
+
 // Tags of one launch: 64 * (launch number) + layer; never 0 (the workspace starts zeroed).
-static uint32_t next_tagbase(mk_model* m) {
+// Also sets the launch's folded O-projection parameters: folded where the context fits one
+// attention unit; the count words alternate between two sets by launch parity, and every launch
+// clears the set the next one uses.
+static uint32_t next_tagbase(mk_model* m, KParams& p) {
   m->steps = (m->steps + 1) & 0x03FFFFFFu;
   if (m->steps == 0) m->steps = 1;
+  p.fold_o = (m->fold_o && p.units == 1) ? 1 : 0;
+  p.wo_rep = m->wo_rep;
+  p.wo_lbytes = m->wo_lbytes;
+  const size_t set = (size_t)m->cfg.n_layers * HID;
+  p.acc = m->acc ? m->acc + (m->steps & 1u) * set : nullptr;
+  p.acc_zero = m->acc ? m->acc + ((m->steps + 1u) & 1u) * set : nullptr;
   return m->steps * 64u;
 }
 
@@ -318,6 +351,7 @@ static int collect_status(mk_model* m, int32_t* next_token) {
   if (st == 4) {
     set_err(m, MK_EINVAL, "a device step read an out-of-range input token");
     cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
+    if (m->acc) cudaMemsetAsync(m->acc, 0, 2 * (size_t)m->cfg.n_layers * HID * sizeof(unsigned long long), m->stream);
     cudaStreamSynchronize(m->stream);
     return MK_EINVAL;
   }
@@ -327,6 +361,7 @@ static int collect_status(mk_model* m, int32_t* next_token) {
             (d >> 16) & 0x7FFF, (d & 0x80000000u) ? " (weight stream)" : "",
             m->host_status[3] ? "; a CTA exited with bulk copies still in flight" : "");
     cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
+    if (m->acc) cudaMemsetAsync(m->acc, 0, 2 * (size_t)m->cfg.n_layers * HID * sizeof(unsigned long long), m->stream);
     cudaStreamSynchronize(m->stream);
     return MK_ETIMEOUT;
   }
@@ -345,8 +380,8 @@ int mk_decode_step(mk_model* m, int32_t token, int32_t pos, int32_t* next_token_
   p.next_out = nullptr;
   p.logits = logits_dev;
   p.units = units_for(m, pos);
-  p.tagbase = next_tagbase(m);
-  if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
+  p.tagbase = next_tagbase(m, p);
+  if (launch_decode(p, m->grid, xray_level(m), m->stream))
     return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
   return collect_status(m, next_token_host);
 }
@@ -363,8 +398,8 @@ int mk_decode_greedy(mk_model* m, int32_t first_token, int32_t pos0, int32_t n, 
     p.next_out = tokens_dev + i;
     p.logits = nullptr;
     p.units = units_for(m, p.pos);
-    p.tagbase = next_tagbase(m);
-    if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
+    p.tagbase = next_tagbase(m, p);
+    if (launch_decode(p, m->grid, xray_level(m), m->stream))
       return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
   }
   return MK_OK;
@@ -380,8 +415,8 @@ int mk_decode_next(mk_model* m, const int32_t* token_dev, int32_t pos, int32_t* 
   p.next_out = next_dev;
   p.logits = logits_dev;
   p.units = units_for(m, pos);
-  p.tagbase = next_tagbase(m);
-  if (launch_decode(p, m->grid, m->trace != nullptr, m->stream))
+  p.tagbase = next_tagbase(m, p);
+  if (launch_decode(p, m->grid, xray_level(m), m->stream))
     return set_err(m, MK_ECUDA, "launch: %s", cudaGetErrorString(cudaGetLastError()));
   return MK_OK;
 }

@@ -223,6 +223,42 @@ int launch_pack_nvfp4_mse(const void* w, int rows, int cols, void* codes, void* 
   return cudaGetLastError() == cudaSuccess ? 0 : -1;
 }
 
+// One layer's W_o [HID rows][QROWS cols] (canonical packed form) -> the folded O-projection's blocks:
+// block (head h, slice s) at dst + (h * FOLD_SLICES + s) * wo_block_bytes(fmt) holds rows
+// [FOLD_ROWS s, +FOLD_ROWS) and columns [HD h, +HD): bf16 / FP8 codes row-major; NVFP4 codes
+// row-major (HD / 2 bytes a row) followed by the rows' E4M3 block scales (HD / 16 bytes a row).
+// One thread per destination byte.
+__global__ void k_repack_o(const uint8_t* __restrict__ data, const uint8_t* __restrict__ scale, int fmt,
+                           uint8_t* __restrict__ dst) {
+  const int bb = wo_block_bytes(fmt);
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)NQH * FOLD_SLICES * bb) return;
+  const int blk = (int)(i / bb), o = (int)(i % bb);
+  const int h = blk / FOLD_SLICES, s = blk % FOLD_SLICES;
+  if (fmt == 2) {
+    const int cb = HD / 2;  // code bytes of a block row
+    if (o < FOLD_ROWS * cb) {
+      const int r = o / cb, c = o % cb;
+      dst[i] = data[(size_t)(FOLD_ROWS * s + r) * (QROWS / 2) + (size_t)cb * h + c];
+    } else {
+      const int o2 = o - FOLD_ROWS * cb, sb = HD / 16;
+      const int r = o2 / sb, c = o2 % sb;
+      dst[i] = scale[(size_t)(FOLD_ROWS * s + r) * (QROWS / 16) + (size_t)sb * h + c];
+    }
+  } else {
+    const int eb = fmt == 0 ? 2 : 1, rb = HD * eb;  // bytes of a block row
+    const int r = o / rb, c = o % rb;
+    dst[i] = data[(size_t)(FOLD_ROWS * s + r) * QROWS * eb + (size_t)rb * h + c];
+  }
+}
+
+int launch_repack_o(const void* data, const void* scale, int fmt, void* dst, void* stream) {
+  const long long n = (long long)NQH * FOLD_SLICES * wo_block_bytes(fmt);
+  k_repack_o<<<(unsigned)((n + 255) / 256), 256, 0, (cudaStream_t)stream>>>((const uint8_t*)data,
+                                                                           (const uint8_t*)scale, fmt, (uint8_t*)dst);
+  return cudaGetLastError() == cudaSuccess ? 0 : -1;
+}
+
 int launch_rope_table(float* cosb, float* sinb, int max_ctx, float theta, void* stream) {
   const int n = max_ctx * (HD / 2);
   k_rope_table<<<(n + 255) / 256, 256, 0, (cudaStream_t)stream>>>(cosb, sinb, max_ctx, (double)theta);

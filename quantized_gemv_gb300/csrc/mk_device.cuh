@@ -58,6 +58,10 @@ __device__ __forceinline__ uint32_t atom_acqrel_add(uint32_t* p, uint32_t v) {
   return old;
 }
 __device__ __forceinline__ void fence_acqrel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+// 64-bit integer add at gpu scope, no return value (count-word contributions).
+__device__ __forceinline__ void red_add_u64(unsigned long long* p, unsigned long long v) {
+  asm volatile("red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 
 // Activations written by other SMs are read at L2 (never through a possibly stale L1 line).
 __device__ __forceinline__ float ld_cg_f32(const float* p) {

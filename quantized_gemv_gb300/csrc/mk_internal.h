@@ -107,7 +107,31 @@ struct KParams {
   unsigned long long timeout_ns;
   int fault_cta;         // test hook (-1 = off)
   int fault_phase;
+  // Folded O-projection (contexts of one attention unit, grid FOLD_GRID): every CTA b runs the
+  // attention of q head b / FOLD_SLICES and multiplies its output by the 128 x 128 block of W_o
+  // whose rows are [128 (b % FOLD_SLICES), +128) and whose columns are that head's; the partial
+  // sums of the 16 heads meet in count words (see acc) that the gate/up step polls in place of
+  // h_attn. 0: attention units and an o_proj GEMV step as above.
+  int fold_o;
+  const uint8_t* wo_rep;   // W_o repacked per (layer, head, slice) block, see wo_block_bytes()
+  size_t wo_lbytes;        // bytes of one layer's blocks
+  unsigned long long* acc;       // count words of this launch [n_layers][HID]
+  unsigned long long* acc_zero;  // the other launch parity's count words, cleared by this launch
 };
+
+// Folded O-projection geometry: 16 q heads x 8 row slices of 128 rows = a grid of 128 CTAs.
+constexpr int FOLD_SLICES = 8;
+constexpr int FOLD_GRID = NQH * FOLD_SLICES;
+constexpr int FOLD_ROWS = HID / FOLD_SLICES;  // 128 output rows per block
+// Bytes of one repacked W_o block (FOLD_ROWS rows x HD columns): bf16 and FP8 codes row-major;
+// NVFP4 codes row-major [128][64 B] followed by the E4M3 block scales [128][8 B].
+__host__ __device__ inline int wo_block_bytes(int fmt) {
+  return fmt == 0 ? FOLD_ROWS * HD * 2 : (fmt == 1 ? FOLD_ROWS * HD : FOLD_ROWS * (HD / 2 + HD / 16));
+}
+// Count words: a contribution v adds ((int64)round(v * 2^24) << 8) + 1 with one 64-bit integer
+// atomic add, so the low byte counts the contributions and the rest holds their fixed-point sum
+// (2^-24 resolution); integer addition makes the result independent of arrival order.
+constexpr float COUNT_SCALE = 16777216.0f;
 
 // CTAs of the persistent decode grid on a device with `sms` SMs (one CTA per SM): 128 where the
 // device has them, so that every CTA's share of each exchanged vector (8 of the 1024 hidden rows,
@@ -116,7 +140,8 @@ struct KParams {
 inline int decode_grid_for(int sms) { return sms >= 128 ? 128 : (sms / NKVH) * NKVH; }
 
 // Launchers (mk_kernel.cu / mk_aux.cu)
-int launch_decode(const KParams& p, int grid, bool xray, void* stream);
+// xray: 0 = plain kernel, 1 = X-ray phase and wait stamps, 2 = stamps and sub-phase marks
+int launch_decode(const KParams& p, int grid, int xray, void* stream);
 int decode_smem_bytes();
 int launch_gemv(const DMat& m, int rows, int cols, const float* x, float* y, int grid, void* stream);
 int launch_stream_read(const void* buf, size_t bytes, int grid, void* stream);
@@ -124,6 +149,7 @@ int launch_rope_table(float* cosb, float* sinb, int max_ctx, float theta, void* 
 int launch_pack_fp8(const void* w, int rows, int cols, void* codes, float* scales, int bf16_scale, void* stream);
 int launch_pack_nvfp4(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
 int launch_pack_nvfp4_mse(const void* w, int rows, int cols, void* codes, void* bscales, float* t, void* stream);
+int launch_repack_o(const void* data, const void* scale, int fmt, void* dst, void* stream);
 int launch_probe_cvt(uint32_t* a, uint32_t* b, const float* in, int n, uint16_t* e4, uint8_t* e2, void* stream);
 int decode_occupancy(int* blocks_per_sm);
 // Record an error text for mk_last_error(NULL) (mk_api.cu).

@@ -49,6 +49,8 @@ struct Sched {
   int hq;        // single-head unit: which q head of the KV group (0 or 1); -1: both heads
   int t0, t1;    // positions [t0, t1) of the chunk
   int ncached;   // positions of the chunk already in the cache (read through the ring)
+  int os;        // folded O-projection: this CTA's slice of W_o rows (FOLD_ROWS each)
+  bool kvw;      // this unit writes the new position's K and V to the cache
   __device__ void make(const KParams& P) {
     const int G = gridDim.x, b = blockIdx.x;
     // q, k and v rows go to disjoint CTA groups in proportion to their sizes (2 : 1 : 1), so every
@@ -68,7 +70,15 @@ struct Sched {
     split_range(FFN, G, b, j0, j1);
     split_range(HID, G, b, d0, d1);
     split_range(P.vocab, G, b, v0, v1);
-    if (P.units == 1) {  // the whole context fits one unit: one unit per q head (16 CTAs)
+    os = 0;
+    if (P.fold_o) {      // folded O-projection: every CTA attends for q head b / 8 (units == 1)
+      unit = true;
+      const int h = b / FOLD_SLICES;
+      os = b % FOLD_SLICES;
+      ug = h / GQA;
+      hq = h % GQA;
+      uc = 0;
+    } else if (P.units == 1) {  // the whole context fits one unit: one unit per q head (16 CTAs)
       unit = b < NQH;
       ug = unit ? b / GQA : 0;
       hq = unit ? b % GQA : 0;
@@ -82,6 +92,8 @@ struct Sched {
     split_range(P.pos + 1, P.units, uc, t0, t1);
     int c_end = t1 < P.pos ? t1 : P.pos;
     ncached = unit ? (c_end > t0 ? c_end - t0 : 0) : 0;
+    // one writer per KV head: the last chunk's unit of the head's first q head (slice 0)
+    kvw = unit && uc == P.units - 1 && hq <= 0 && os == 0;
   }
 };
 
@@ -103,7 +115,8 @@ struct __align__(16) Smem {
   float xs[XS_MAX];
   float hs[HID];
   float red[64];
-  float qs[2][HD];
+  float qs[2][HD];                   // attention: q of the unit's heads; with the folded O-projection
+                                     // (one head a CTA) qs[1] holds the head's output instead
   float kn[HD];
   float vn[HD];
   float sc[2][UNIT_POS];
@@ -152,7 +165,8 @@ __device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float((uin
 __device__ __forceinline__ float ldg_bf16(const uint16_t* p) { return bf16f(__ldg(p)); }
 
 // ------------------------------------------------------------------ X-ray
-template <bool XR>
+// XR: 0 = no X-ray, 1 = phase and wait stamps, 2 = stamps and sub-phase marks.
+template <int XR>
 struct Xray {
   TraceRec* base;
   int n;
@@ -161,7 +175,7 @@ struct Xray {
     n = 0;
   }
   __device__ __forceinline__ void stamp(int phase, int kind) {
-    if (XR && base && n < TRACE_PER_CTA) {
+    if (XR >= 1 && base && n < TRACE_PER_CTA) {
       TraceRec r;
       r.gtime = globaltimer();
       r.clk = clock64_();
@@ -175,7 +189,7 @@ struct Xray {
   // Sub-phase mark (kind 4): the SM clock only (reading %globaltimer costs far more than clock64
   // and would distort the short intervals the marks resolve); gtime = 0, smid = 0.
   __device__ __forceinline__ void mark(int id) {
-    if (XR && base && n < TRACE_PER_CTA) {
+    if (XR >= 2 && base && n < TRACE_PER_CTA) {
       unsigned long long* w = reinterpret_cast<unsigned long long*>(base + n++);
       w[0] = 0ull;
       w[1] = clock64_();
@@ -183,7 +197,7 @@ struct Xray {
     }
   }
   __device__ void finish() {
-    if (XR && base && n < TRACE_PER_CTA) {
+    if (XR >= 1 && base && n < TRACE_PER_CTA) {
       TraceRec r = {};
       r.kind = 255;  // end marker
       base[n] = r;
@@ -258,6 +272,13 @@ struct Producer {
             (uint32_t)(nr * sb));
     }
   }
+  // The W_o block of (head, slice) of layer `layer` for the folded O-projection: one tile
+  // (FP8, NVFP4) or two tiles of 64 rows (bf16).
+  __device__ void wo_block(int layer, int h, int sl, int fmt) {
+    const int bb = wo_block_bytes(fmt);
+    const uint8_t* src = P->wo_rep + (size_t)layer * P->wo_lbytes + (size_t)(h * FOLD_SLICES + sl) * bb;
+    for (int o = 0; o < bb && ok; o += SLOT) issue(src + o, (uint32_t)min(SLOT, bb - o), nullptr, 0);
+  }
   __device__ void kv(int layer, int g, int t0, int ncached) {
     for (int t = 0; t < ncached && ok; t += KVT) {
       int np = min(KVT, ncached - t);
@@ -311,7 +332,8 @@ __device__ void run_producer(const KParams& P, Smem* s, uint8_t* ring) {
     const DLayer& L = P.layers[l];
     pr.rows(L.m[M_Q + S.qm], HID, S.qr0, S.qr1);
     if (S.unit) pr.kv(l, S.ug, S.t0, S.ncached);
-    pr.rows(L.m[M_O], QROWS, S.o0, S.o1);
+    if (P.fold_o) pr.wo_block(l, S.ug * GQA + S.hq, S.os, L.m[M_O].fmt);
+    else pr.rows(L.m[M_O], QROWS, S.o0, S.o1);
     pr.rows_paired(L.m[M_GATE], L.m[M_UP], HID, S.j0, S.j1);
     pr.rows(L.m[M_DOWN], FFN, S.d0, S.d1);
   }
@@ -329,7 +351,7 @@ __device__ __forceinline__ void ld_ll2(const llword* p, llword& a, llword& b) {
   asm volatile("ld.relaxed.gpu.global.v2.b64 {%0,%1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
 }
 
-template <bool XR>
+template <int XR>
 struct Consumer {
   Smem* s;
   uint8_t* ring;
@@ -360,7 +382,7 @@ struct Consumer {
   // going to the next CTA barrier, where the abort is seen by every warp).
   __device__ void wait_full(uint32_t slot, uint32_t par, int phase, int layer) {
     if (mbar_test_wait(&s->full[slot], par)) return;
-    if (XR && warp == 0 && lane == 0) xr.mark(54);  // X-ray: a tile was not there yet
+    if (XR >= 2 && warp == 0 && lane == 0) xr.mark(54);  // X-ray: a tile was not there yet
     uint64_t t0 = globaltimer();
     while (!mbar_try_wait(&s->full[slot], par)) {  // suspends the warp for a while in hardware
       if (s->abort) return;
@@ -384,18 +406,25 @@ struct Consumer {
     geom_rt(fmt, K, rpt, mag);
     return (paired ? 2 : 1) * (int)__umulhi((uint32_t)(nrows + rpt - 1), mag);
   }
-  // Wait for the nwords LL words at src (tag), two per thread per round, and stage them:
+  // Wait for the nwords words at src, two per thread per round, and stage them. The words are
+  // LL words carrying `tag` (cnt == 0), or count words (cnt > 0: ready once their low byte equals
+  // cnt; the value is hs[k] plus their fixed-point sum, i.e. the residual this CTA staged last
+  // plus the folded partial sums). Staging:
   //  normed: hs[k] = h[k], xs[k] = h[k] * w[k] (w = this thread's two bf16 norm weights of elements
   //          2 tid, 2 tid + 1, loaded before the wait), and red[warp] = the warp's sum of h^2;
   //  plain:  xs[k] = x[k].
   // xs is laid out for a matrix of format fmt. hook() runs before the closing CTA barrier.
   template <class Hook>
   __device__ bool poll_stage(const llword* src, int nwords, uint32_t tag, int phase, int layer, bool normed, uint2 wb,
-                             int fmt, int res_tiles, Hook hook) {
+                             int fmt, int res_tiles, Hook hook, int cnt = 0) {
     if (tid == 0) xr.stamp(phase, 2);
     const int epl = epl_of(fmt);
     constexpr int MAXW = (FFN + 2 * NCT - 1) / (2 * NCT);  // word pairs per thread, at most
     const int nw = (nwords - 2 * tid + 2 * NCT - 1) / (2 * NCT);
+    const uint64_t want = cnt ? (uint64_t)cnt : (uint64_t)tag;
+    const int sh = cnt ? 0 : 32;
+    const uint64_t msk = cnt ? 0xFFull : 0xFFFFFFFFull;
+    auto rdy = [&](llword w) { return ((w >> sh) & msk) == want; };
     llword a[MAXW], b[MAXW];
     // every load of this thread goes out at once; only the late ones are polled again
 #pragma unroll
@@ -405,7 +434,7 @@ struct Consumer {
     bool ready = true;
 #pragma unroll
     for (int i = 0; i < MAXW; ++i)
-      if (i < nw) ready = ready && ll_tag(a[i]) == tag && ll_tag(b[i]) == tag;
+      if (i < nw) ready = ready && rdy(a[i]) && rdy(b[i]);
     if (!ready) {
       const uint64_t t0 = globaltimer();
       uint32_t it = 0;
@@ -413,9 +442,9 @@ struct Consumer {
         ready = true;
 #pragma unroll
         for (int i = 0; i < MAXW; ++i) {
-          if (i < nw && (ll_tag(a[i]) != tag || ll_tag(b[i]) != tag)) {
+          if (i < nw && (!rdy(a[i]) || !rdy(b[i]))) {
             ld_ll2(src + 2 * tid + 2 * NCT * i, a[i], b[i]);
-            ready = ready && ll_tag(a[i]) == tag && ll_tag(b[i]) == tag;
+            ready = ready && rdy(a[i]) && rdy(b[i]);
           }
         }
         if (ready) break;
@@ -436,7 +465,14 @@ struct Consumer {
     for (int i = 0; i < MAXW; ++i) {
       if (i >= nw) break;
       const int k = 2 * tid + 2 * NCT * i;
-      const float va = ll_val(a[i]), vb = ll_val(b[i]);
+      float va, vb;
+      if (cnt) {
+        va = s->hs[k] + __ll2float_rn((long long)a[i] >> 8) * (1.0f / COUNT_SCALE);
+        vb = s->hs[k + 1] + __ll2float_rn((long long)b[i] >> 8) * (1.0f / COUNT_SCALE);
+      } else {
+        va = ll_val(a[i]);
+        vb = ll_val(b[i]);
+      }
       if (normed) {
         const uint32_t wbits = i == 0 ? wb.x : wb.y;
         s->hs[k] = va;
@@ -856,6 +892,52 @@ struct Consumer {
     }
   }
 
+  // ---------------------------------------------------------------- folded O-projection
+  // This CTA's block of W_o (rows [FOLD_ROWS S.os, +FOLD_ROWS), the columns of its q head) times
+  // the head's attention output (qs[1]), added into the count words acc[l][row] (one atomic a row, 16
+  // contributions a row over the grid). Warp w takes block rows [16 w, 16 w + 16); a row's bytes
+  // split into 16-byte chunks over LPR lanes, 32 / LPR rows a pass, then a shuffle reduction over
+  // the LPR lanes. The block's tiles are resident (waited for by the caller).
+  template <int FMT>
+  __device__ void fold_o_rows(const KParams& p, const DMat& mo, int l, bool skip) {
+    constexpr int EPL = FMT == 0 ? 8 : (FMT == 1 ? 16 : 32);             // elements per 16-byte chunk
+    constexpr int LPR = HD / EPL;                                         // lanes per row: 16, 8, 4
+    constexpr int RPI = 32 / LPR;                                         // rows per pass
+    constexpr int ROWB = FMT == 0 ? HD * 2 : (FMT == 1 ? HD : HD / 2);    // code bytes per block row
+    const int c = lane % LPR, rsub = lane / LPR;
+    float4 x[EPL / 4];
+#pragma unroll
+    for (int j = 0; j < EPL / 4; ++j) x[j] = reinterpret_cast<const float4*>(s->qs[1])[c * (EPL / 4) + j];
+    const int r0 = FOLD_ROWS * S_os;
+#pragma unroll
+    for (int pass = 0; pass < 16 / RPI; ++pass) {
+      const int r = 16 * warp + RPI * pass + rsub;  // block row
+      // a bf16 block spans two tiles of 64 rows; FP8 and NVFP4 blocks fill one tile
+      const uint8_t* tile = ring + (size_t)((n + (FMT == 0 ? (r >> 6) : 0)) % NSLOT) * SLOT;
+      const uint8_t* row = tile + (size_t)(FMT == 0 ? (r & 63) : r) * ROWB;
+      const uint4 w = *reinterpret_cast<const uint4*>(row + 16 * c);
+      float acc[2] = {0.f, 0.f};
+      if constexpr (FMT == 0) {
+        dot_bf16_16B(w, x, acc);
+      } else if constexpr (FMT == 1) {
+        dot_fp8_16B(w, x, acc);
+      } else {
+        const uint16_t bs2 = *reinterpret_cast<const uint16_t*>(tile + FOLD_ROWS * ROWB + r * (HD / 16) + 2 * c);
+        const float2 bs = e4m3x2_to_f2(bs2);
+        dot_nvfp4_16B(w, x, bs.x, bs.y, acc);
+      }
+      float v = acc[0] + acc[1];
+#pragma unroll
+      for (int o = LPR / 2; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (c == 0 && !skip) {
+        const float sc = FMT == 1 ? __ldg(reinterpret_cast<const float*>(mo.scale) + r0 + r) : (FMT == 2 ? mo.tscale : 1.f);
+        const long long f = __float2ll_rn(v * sc * COUNT_SCALE);
+        red_add_u64(p.acc + (size_t)l * HID + r0 + r, ((unsigned long long)f << 8) + 1ull);
+      }
+    }
+  }
+  int S_os;  // this CTA's W_o row slice (folded O-projection), copied from the schedule
+
   // One attention unit: KV head g, positions [S.t0, S.t1) of layer l; q head 2g + S.hq alone
   // (S.hq >= 0) or both q heads of the group.
   __device__ bool attention(const Sched& S, const DLayer& L, int l, uint32_t tag) {
@@ -934,7 +1016,7 @@ struct Consumer {
         for (int j = 0; j < 4; ++j) {
           const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
           v[j] = bf16f(bits);
-          if (S.uc == p.units - 1 && S.hq <= 0) cache[row + lane + 32 * j] = bits;
+          if (S.kvw) cache[row + lane + 32 * j] = bits;
           (warp == 2 ? s->knew : s->vnew)[lane + 32 * j] = bits;
         }
       }
@@ -1094,7 +1176,9 @@ struct Consumer {
         lsum = fmaf(f, s->wst[w][2 + h], lsum);
         acc = fmaf(f, wo[(w * 2 + h) * HD + d], acc);
       }
-      if (p.units == 1) {  // one unit covers the whole context: no merge needed
+      if (p.fold_o) {  // folded O-projection: the head's output stays in this CTA
+        s->qs[1][d] = acc / lsum;
+      } else if (p.units == 1) {  // one unit covers the whole context: no merge needed
         const int oh = HEADS == 2 ? h : S.hq;  // q head of the group this output belongs to
         if (!faulted(PH_ATTN, l)) ll_store(p.att + GQA * HD * g + oh * HD + d, tag, acc / lsum);
       } else {
@@ -1106,7 +1190,7 @@ struct Consumer {
         }
       }
     }
-    if (p.units == 1) return true;
+    if (p.units == 1 || p.fold_o) return true;
     bar_consumers(NCT);
     // the last unit of this KV head to finish merges the chunks
     if (tid == 0) {
@@ -1141,6 +1225,10 @@ struct Consumer {
       if (tid != ST_ATTN) make_step(tid, p, S0, s->steps[tid]);
     }
     const Sched& S = s->sched;
+    if (p.acc_zero) {  // the next launch's count words (this launch reads the other set)
+      const int total = p.n_layers * HID;
+      for (int i = blockIdx.x * NCT + tid; i < total; i += G * NCT) p.acc_zero[i] = 0ull;
+    }
     // ---------------- embedding: h = row `token` of the tied matrix (every CTA, no wait)
     st(PH_EMBED, 0);
     const int token = p.token_ptr ? *(volatile const int32_t*)p.token_ptr : p.token;
@@ -1194,8 +1282,25 @@ struct Consumer {
             if (!attention(S, L, l, tag)) return;
             st(PH_ATTN, 1);
           }
+          if (p.fold_o) {  // the O-projection of this CTA's head and row slice, into count words
+            st(PH_O, 0);
+            const DMat mo = L.m[M_O];
+            const int wt = (wo_block_bytes(mo.fmt) + SLOT - 1) / SLOT;
+            wait_tiles(0, wt, PH_O, l);
+            bar_consumers(NCT);  // publishes the head output and the landed tiles
+            if (s->abort) return;
+            S_os = S.os;
+            const bool skip = faulted(PH_ATTN, l);
+            if (mo.fmt == 0) fold_o_rows<0>(p, mo, l, skip);
+            else if (mo.fmt == 1) fold_o_rows<1>(p, mo, l, skip);
+            else fold_o_rows<2>(p, mo, l, skip);
+            warp_release_tiles(0, wt);
+            n += wt;
+            st(PH_O, 1);
+          }
           continue;
         }
+        if (step == ST_O && p.fold_o) continue;  // folded into the attention step
         // ---- the step: everything that does not change with the layer comes from the table
         const StepDesc& d = s->steps[step];
         const DMat ma = d.mi < 0 ? p.embed : L.m[d.mi];
@@ -1244,6 +1349,10 @@ struct Consumer {
           resident_wait(res ? ntiles : 0);
           bar_consumers(NCT);
           if (s->abort) return;
+        } else if (step == ST_GU && p.fold_o) {  // h_attn = the staged residual + the 16 heads' partial sums
+          if (!poll_stage(reinterpret_cast<const llword*>(p.acc + (size_t)l * HID), HID, 0u, d.wait_phase, l, normed,
+                          wb, fmt, res ? ntiles : 0, [] {}, NQH))
+            return;
         } else if (!poll_stage(d.src, d.nsrc, tag - (uint32_t)d.stag_m1, d.wait_phase, l, normed, wb, fmt,
                                res ? ntiles : 0, [] {})) {
           return;
@@ -1302,7 +1411,7 @@ struct Consumer {
   }
 };
 
-template <bool XR>
+template <int XR>
 __global__ void __launch_bounds__(NTHREADS, 1) k_decode(const KParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* ring = smem_raw;
@@ -1370,7 +1479,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
     pr.rows(m, cols, r0, r1);
     if (!pr.ok) pr.drain();
   } else {
-    Consumer<false> c;
+    Consumer<0> c;
     c.s = s;
     c.ring = ring;
     c.P = &p;
@@ -1381,15 +1490,15 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_gemv(const DMat m, int rows, in
     c.eps = 0.f;
     c.xr.init(nullptr);
     c.stage_global(x, cols, m.fmt);
-    typename Consumer<false>::EpiCtx e;
-    e.kind = Consumer<false>::EPI_OUT;
+    typename Consumer<0>::EpiCtx e;
+    e.kind = Consumer<0>::EPI_OUT;
     e.tag = 0;
     e.skip = false;
     e.inv = 1.f;
     e.ll = nullptr;
     e.fout = y;
     e.dbg = nullptr;
-    typename Consumer<false>::Plan pl;
+    typename Consumer<0>::Plan pl;
     if (r0 < r1) c.plan_first(false, m, m, r0, r1, cols, pl);
     c.gemv(false, m, m, r0, r1, cols, pl, e, false);
     bar_consumers(NCT);
@@ -1459,9 +1568,11 @@ static int set_attrs() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_ATTR_DEVICES) return -1;
   if (g_attr_done[dev]) return 0;
   cudaError_t e;
-  e = cudaFuncSetAttribute(k_decode<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = cudaFuncSetAttribute(k_decode<0>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return -1;
-  e = cudaFuncSetAttribute(k_decode<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  e = cudaFuncSetAttribute(k_decode<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e != cudaSuccess) return -1;
+  e = cudaFuncSetAttribute(k_decode<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return -1;
   e = cudaFuncSetAttribute(k_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) return -1;
@@ -1473,16 +1584,17 @@ static int set_attrs() {
 
 int decode_occupancy(int* blocks_per_sm) {
   if (set_attrs()) return -1;
-  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_decode<false>, NTHREADS, SMEM_BYTES) ==
+  return cudaOccupancyMaxActiveBlocksPerMultiprocessor(blocks_per_sm, k_decode<0>, NTHREADS, SMEM_BYTES) ==
                  cudaSuccess
              ? 0
              : -1;
 }
 
-int launch_decode(const KParams& p, int grid, bool xray, void* stream) {
+int launch_decode(const KParams& p, int grid, int xray, void* stream) {
   if (set_attrs()) return -1;
   void* args[] = {(void*)&p};
-  cudaError_t e = cudaLaunchCooperativeKernel(xray ? (const void*)k_decode<true> : (const void*)k_decode<false>,
+  const void* fn = xray >= 2 ? (const void*)k_decode<2> : (xray == 1 ? (const void*)k_decode<1> : (const void*)k_decode<0>);
+  cudaError_t e = cudaLaunchCooperativeKernel(fn,
                                               dim3(grid), dim3(NTHREADS), args, SMEM_BYTES, (cudaStream_t)stream);
   return e == cudaSuccess ? 0 : -1;
 }

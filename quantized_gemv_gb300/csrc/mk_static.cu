@@ -142,7 +142,7 @@ int mk_decode_step_static(const mk_config* c, const mk_weights* w, void* kv_k_de
   p.timeout_ns = 500000000ull;
   p.fault_cta = -1;
   p.fault_phase = -1;
-  if (launch_decode(p, D.grid, false, st)) return fail(MK_ECUDA, cudaGetErrorString(cudaGetLastError()));
+  if (launch_decode(p, D.grid, 0, st)) return fail(MK_ECUDA, cudaGetErrorString(cudaGetLastError()));
   // the step's status and token (SyncBlock::status then ::tok, 64 words)
   uint32_t hs[64];
   e = cudaMemcpyAsync(hs, S->sync.status, sizeof hs, cudaMemcpyDeviceToHost, st);

@@ -17,6 +17,8 @@ from .synthetic import FMT_BF16, FMT_FP8_ROW, FMT_NVFP4, LINEARS, ModelConfig
 
 MK_OK, MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, MK_ENOTRACE = 0, -1, -2, -3, -4, -5
 MK_FLAG_XRAY = 1
+MK_FLAG_XRAY_MARKS = 4
+MK_FLAG_NO_FOLD = 8
 ERRNAMES = {MK_EINVAL: "MK_EINVAL", MK_ECUDA: "MK_ECUDA", MK_ETIMEOUT: "MK_ETIMEOUT",
             MK_ENORESIDENT: "MK_ENORESIDENT", MK_ENOTRACE: "MK_ENOTRACE"}
 TRACE_DTYPE = np.dtype([("gtime", "<u8"), ("clk", "<u8"), ("smid", "<u4"), ("cta", "<u2"),
