@@ -60,7 +60,7 @@ def test_instrumented_build_matches_plain_build():
     master = S.master_weights(cfg, seed=61)
     packed = mk.pack_model(master, S.format_map("fp8"))
     plain = mk.Model(cfg, packed)
-    xr = mk.Model(cfg, packed, flags=mk.MK_FLAG_XRAY)
+    xr = mk.Model(cfg, packed, flags=mk.MK_FLAG_XRAY | mk.MK_FLAG_XRAY_MARKS)
     tok = 3
     for pos in range(6):  # teacher-forced on the plain build's tokens
         lp = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
@@ -147,3 +147,38 @@ def test_critical_path_three_layers():
     assert cp["exchange_qkv_last"] == (1500 + 5) - (1110 + 340)
     assert cp["phase_qkv"] == (1510 + 100) - (1500 + 5)
     assert cp["layer"] == 400
+
+
+@pytest.mark.gpu
+def test_stamps_only_build_has_no_marks_and_spans_the_launch():
+    """MK_FLAG_XRAY alone records phase and wait stamps only (no sub-phase marks), and on a
+    28-layer model the span from the first to the last stamp of a step is within 5 % of that
+    launch's CUDA-event time inside a back-to-back run (the X-ray milestone's check that the
+    phases account for the token)."""
+    from quantized_gemv_gb300 import mk
+    from quantized_gemv_gb300 import synthetic as S
+
+    cfg = S.ModelConfig(n_layers=28, vocab=4099, max_ctx=256)
+    packed = mk.pack_model(S.master_weights(cfg, seed=62), S.format_map("bf16"))
+    xr = mk.Model(cfg, packed, flags=mk.MK_FLAG_XRAY)
+    n = 8
+    toks = torch.zeros(n + 1, dtype=torch.int32, device="cuda")
+    toks[0] = 5
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    torch.cuda.synchronize()
+    with torch.cuda.stream(xr.stream):
+        for i in range(n):
+            ev[i].record(xr.stream)
+            xr.decode_next(toks[i: i + 1], i, toks[i + 1: i + 2])
+        ev[n].record(xr.stream)
+    xr.sync()
+    launch_ns = ev[n - 1].elapsed_time(ev[n]) * 1e6
+    tr = xr.trace()
+    kinds = set()
+    for c in range(tr.shape[0]):
+        stop = np.flatnonzero(tr[c]["kind"] == STOP)
+        kinds |= set(np.unique(tr[c][: stop[0]]["kind"]).tolist())
+    assert MARK not in kinds
+    span = xray.analyze(tr)["token_ns"]
+    assert 0.95 * launch_ns <= span <= launch_ns, (span, launch_ns)
+    xr.close()
