@@ -399,6 +399,46 @@ def run_sweep(mk, steps: int = 32, warmup: int = 3):
             "data": "synthetic (seeded N(0,0.02) weights; KV cache prefilled N(0,1) bf16)", "sweep": rows}
 
 
+def run_verify(mk, name: str = HEADLINE, ks=(1, 2, 4, 8), launches: int = 16, warmup: int = 3):
+    """The batched verify step (tensor cores): verified tokens per second for k tokens a launch, on
+    the workload's model after its prompt; launch i verifies k seeded uniform-random tokens at
+    positions P + i k .. P + i k + k - 1. Each launch reads every weight once (the 16-bit copy the
+    verify step streams), so its weight stream is reported against the measured copy bandwidth."""
+    wl = S.WORKLOADS[name]
+    cfg, _, model, pos0, _ = setup_model(wl, mk)
+    model.verify_attach()
+    stream = model.stream
+    toks = torch.tensor(S.prompt_ids(cfg, 8 * (launches + warmup), seed=5), dtype=torch.int32, device="cuda")
+    nxt = torch.zeros(8, dtype=torch.int32, device="cuda")
+    vbytes = 2 * sum(r * c for r, c in cfg.shapes().values()) * cfg.n_layers + 2 * cfg.vocab * cfg.hidden
+    peak, _ = measured_peaks()
+    rows = []
+    for k in ks:
+        if pos0 + k * (launches + warmup) > min(cfg.max_ctx, 1024):
+            continue
+        for i in range(warmup):
+            model.verify_step(toks[k * i: k * i + k], pos0 + k * i, nxt[:k])
+        model.sync()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(launches + 1)]
+        torch.cuda.synchronize()
+        with torch.cuda.stream(stream):
+            for i in range(launches):
+                ev[i].record(stream)
+                model.verify_step(toks[k * i: k * i + k], pos0 + k * i, nxt[:k])
+            ev[launches].record(stream)
+        model.sync()
+        per = [ev[i].elapsed_time(ev[i + 1]) for i in range(launches)]
+        ms = ev[0].elapsed_time(ev[launches]) / launches
+        gbs = vbytes / (float(np.mean(per)) * 1e-3) / 1e9
+        rows.append({"k": k, "verified_tok_s": round(k / (ms * 1e-3), 1), "ms_per_launch": round(ms, 4),
+                     "weight_gbs": round(gbs, 1), "frac_of_measured_hbm": round(gbs / peak, 4),
+                     "positions": f"{pos0}..{pos0 + k * launches - 1}"})
+    model.close()
+    return {"workload": name, "launches": launches, "warmup": warmup, "weight_bytes_per_launch": vbytes,
+            "note": "one launch per k tokens (tcgen05 GEMMs, fp32 accumulation); tokens seeded uniform, "
+                    "so this measures verify throughput, not an acceptance rate", "rows": rows}
+
+
 def run_workload(wl: S.Workload, steps: int, warmup: int, mk, dist=None, e2e_steps: int | None = None,
                  runs: int = 5):
     """The contract's timed region of `steps` launches, then `runs` more regions of the same
@@ -494,6 +534,7 @@ def main():
     ap.add_argument("--sweep", action="store_true", help="print the context-length sweep (FP8) alone")
     ap.add_argument("--no-sweep", action="store_true", help="leave the context-length sweep out of the line")
     ap.add_argument("--no-layer1", action="store_true", help="leave the one-layer workload out of the line")
+    ap.add_argument("--no-verify", action="store_true", help="leave the batched verify step out of the line")
     ap.add_argument("--cpu-leg", action="store_true", help=argparse.SUPPRESS)  # internal: the oracle leg
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help=argparse.SUPPRESS)
     ap.add_argument("--cpu-seconds-1t", type=float, default=10.0, help=argparse.SUPPRESS)
@@ -565,6 +606,7 @@ def main():
                                   plain_tok_s=v["runs"]["median_tok_s"] if v else None)
             xr = {"headline": xr, "qwen3_0.6b_fp8_ctx4096": xr_ctx}
     layer1 = run_layer1(mk) if rank == 0 and not args.no_layer1 else None
+    verify = run_verify(mk) if rank == 0 and not args.no_verify else None
     sweep = run_sweep(mk) if rank == 0 and not args.no_sweep else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -605,6 +647,7 @@ def main():
         "xray": xr,
         "variants": variants,
         "layer1_bf16": layer1,
+        "verify": verify,
         "sweep": sweep["sweep"] if sweep else None,
     }
     print(json.dumps(line))

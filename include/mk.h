@@ -220,6 +220,38 @@ int mk_stream_read(const void* buf_dev, size_t bytes, void* stream);
 int mk_probe_cvt(uint32_t* f16_from_e4m3_dev, uint32_t* f16_from_e2m1_dev, const float* in_dev, int n,
                  uint16_t* e4m3_from_f32_dev, uint8_t* e2m1_from_f32_dev, void* stream);
 
+/* ---------------------------------------------------------------- batched verify
+ * The batched speculative-verify step (monolith page, "Upstream facts", tensor cores and ISA, and
+ * the throughput bullets: batch-1 decode does not use tensor cores, a batched verify would): k given
+ * tokens at positions pos0 .. pos0 + k - 1 run through every layer and the LM head in ONE persistent
+ * launch that reads each weight byte once for all k, with the GEMMs on the tcgen05 tensor cores
+ * (bf16 layers as bf16; FP8 and NVFP4 layers as their exact f16 values; every activation split into
+ * a 16-bit high and low part, fp32 accumulation), causal attention over the k new positions, and
+ * one argmax per position. The result is what k teacher-forced mk_decode_step calls give, within
+ * the parity tolerances; the keys and values of the k positions are written to the model's cache. */
+
+/* Most tokens one verify launch takes. */
+#define MK_VERIFY_MAX 8
+
+/* Bytes of device workspace mk_verify_attach needs for model m (a 16-bit repacked copy of every
+ * weight matrix laid out for the tensor cores, about 2 bytes per weight, plus exchange buffers). */
+size_t mk_verify_workspace_bytes(const mk_model* m);
+
+/* Prepare m for mk_verify_step: repack its weights into workspace_dev (caller-owned, at least
+ * mk_verify_workspace_bytes(m) bytes, 16-byte aligned; it must outlive m). Needs the decode grid of
+ * 128 CTAs (MK_ENORESIDENT otherwise) and layers that are all bf16 or all quantised (MK_EINVAL).
+ * Synchronises the model's stream. */
+int mk_verify_attach(mk_model* m, void* workspace_dev, size_t workspace_bytes);
+
+/* One verify launch: tokens_dev (device int32 [k], 1 <= k <= MK_VERIFY_MAX) are the inputs at
+ * positions pos0 .. pos0 + k - 1 (pos0 + k <= max_ctx and <= 1024; positions < pos0 must be in the
+ * cache); next_dev (device int32 [k]) receives the argmax after each position (lowest index among
+ * equal maxima) and logits_dev, if not NULL, the fp32 logits [k][vocab]. Does not synchronise;
+ * device-side errors are reported by the next mk_sync. MK_EINVAL for bad arguments or a model
+ * without mk_verify_attach. */
+int mk_verify_step(mk_model* m, const int32_t* tokens_dev, int32_t k, int32_t pos0, int32_t* next_dev,
+                   float* logits_dev);
+
 /* ---------------------------------------------------------------- allocation-free step */
 
 /* Largest max_ctx mk_decode_step_static accepts. */

@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "mk_host.h"
+#include "mk_verify.h"
 
 using namespace mk;
 
@@ -38,6 +39,13 @@ struct mk_model {
   unsigned long long timeout_ns;
   int fault_cta, fault_phase;
   std::string err;
+  // batched verify (mk_verify_attach)
+  std::vector<DLayer> hlayers;  // host copy of the layer table
+  uint8_t* vw = nullptr;        // repacked layer blocks
+  uint8_t* vhead = nullptr;     // repacked LM-head blocks
+  uint32_t* vx = nullptr;       // two sentinel exchange sets (launch parity)
+  int vlayer_bf16 = 0, vhead_bf16 = 0;
+  uint32_t vsteps = 0;
 };
 
 static thread_local std::string g_create_err;
@@ -224,6 +232,7 @@ int mk_create(const mk_config* c, const mk_weights* w, void* ws, size_t ws_bytes
   if ((rc = check_weights(c, w, dl.data())) != MK_OK) return rc;
 
   mk_model* m = new mk_model();
+  m->hlayers = dl;
   m->cfg = *c;
   m->flags = flags;
   m->stream = (cudaStream_t)stream;
@@ -352,6 +361,7 @@ static int collect_status(mk_model* m, int32_t* next_token) {
     set_err(m, MK_EINVAL, "a device step read an out-of-range input token");
     cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
     if (m->acc) cudaMemsetAsync(m->acc, 0, 2 * (size_t)m->cfg.n_layers * HID * sizeof(unsigned long long), m->stream);
+    if (m->vx) cudaMemsetAsync(m->vx, 0xFF, 2 * v_x_words(m->cfg.n_layers) * sizeof(uint32_t), m->stream);
     cudaStreamSynchronize(m->stream);
     return MK_EINVAL;
   }
@@ -362,6 +372,7 @@ static int collect_status(mk_model* m, int32_t* next_token) {
             m->host_status[3] ? "; a CTA exited with bulk copies still in flight" : "");
     cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
     if (m->acc) cudaMemsetAsync(m->acc, 0, 2 * (size_t)m->cfg.n_layers * HID * sizeof(unsigned long long), m->stream);
+    if (m->vx) cudaMemsetAsync(m->vx, 0xFF, 2 * v_x_words(m->cfg.n_layers) * sizeof(uint32_t), m->stream);
     cudaStreamSynchronize(m->stream);
     return MK_ETIMEOUT;
   }
@@ -459,6 +470,94 @@ int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms) {
   m->fault_cta = cta;
   m->fault_phase = phase;
   if (timeout_ms > 0) m->timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
+  return MK_OK;
+}
+
+// ------------------------------------------------------------------ batched verify
+// Workspace layout of the verify path: repacked layer blocks, repacked LM-head blocks, two sentinel
+// exchange sets.
+static size_t verify_layout(const mk_model* m, size_t* head_off, size_t* x_off) {
+  const size_t lw = align_up((size_t)m->cfg.n_layers * v_layer_bytes(), 256);
+  const size_t hw = align_up((size_t)V_GRID * v_head_cta_bytes(m->cfg.vocab), 256);
+  if (head_off) *head_off = lw;
+  if (x_off) *x_off = lw + hw;
+  return lw + hw + 2 * v_x_words(m->cfg.n_layers) * sizeof(uint32_t);
+}
+
+size_t mk_verify_workspace_bytes(const mk_model* m) { return m ? verify_layout(m, nullptr, nullptr) : 0; }
+
+int mk_verify_attach(mk_model* m, void* ws, size_t ws_bytes) {
+  if (!m) return MK_EINVAL;
+  if (m->grid != V_GRID) return set_err(m, MK_ENORESIDENT, "the verify step needs a decode grid of %d CTAs", V_GRID);
+  // one operand type per part: bf16 matrices stay bf16, FP8 and NVFP4 ones become exact f16
+  const int lb = m->hlayers[0].m[0].fmt == MK_BF16;
+  for (const DLayer& L : m->hlayers)
+    for (int i = 0; i < 7; ++i)
+      if ((L.m[i].fmt == MK_BF16) != (lb != 0))
+        return set_err(m, MK_EINVAL, "verify: the layers mix bf16 and quantised matrices");
+  size_t head_off, x_off;
+  const size_t need = verify_layout(m, &head_off, &x_off);
+  if (!ws || ws_bytes < need || !aligned16(ws))
+    return set_err(m, MK_EINVAL, "verify workspace too small or unaligned (%zu < %zu)", ws_bytes, need);
+  uint8_t* base = (uint8_t*)ws;
+  m->vw = base;
+  m->vhead = base + head_off;
+  m->vx = (uint32_t*)(base + x_off);
+  m->vlayer_bf16 = lb;
+  m->vhead_bf16 = m->embed.fmt == MK_BF16;
+  m->vsteps = 0;
+  cudaError_t e = cudaSuccess;
+  for (int l = 0; l < m->cfg.n_layers && e == cudaSuccess; ++l)
+    if (launch_verify_repack_layer(m->hlayers[l], lb, m->vw + (size_t)l * v_layer_bytes(), m->stream))
+      e = cudaGetLastError();
+  if (e == cudaSuccess && launch_verify_repack_head(m->embed, m->cfg.vocab, m->vhead_bf16, m->vhead, m->stream))
+    e = cudaGetLastError();
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(m->vx, 0xFF, 2 * v_x_words(m->cfg.n_layers) * sizeof(uint32_t), m->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(m->stream);
+  if (e != cudaSuccess) {
+    m->vw = nullptr, m->vhead = nullptr, m->vx = nullptr;
+    return set_err(m, MK_ECUDA, "mk_verify_attach: %s", cudaGetErrorString(e));
+  }
+  return MK_OK;
+}
+
+int mk_verify_step(mk_model* m, const int32_t* tokens_dev, int32_t k, int32_t pos0, int32_t* next_dev,
+                   float* logits_dev) {
+  if (!m || !tokens_dev || !next_dev) return MK_EINVAL;
+  if (!m->vw) return set_err(m, MK_EINVAL, "mk_verify_attach was not called");
+  if (k < 1 || k > VK) return set_err(m, MK_EINVAL, "k = %d outside 1..%d", k, VK);
+  if (pos0 < 0 || (long long)pos0 + k > m->cfg.max_ctx || pos0 + k > V_MAXPOS)
+    return set_err(m, MK_EINVAL, "positions %d..%d outside the cache or the verify window (%d)", pos0, pos0 + k - 1,
+                   V_MAXPOS);
+  VParams p = {};
+  p.layers = m->dlayers;
+  p.n_layers = m->cfg.n_layers;
+  p.embed = m->embed;
+  p.final_norm = m->final_norm;
+  p.vocab = m->cfg.vocab;
+  p.max_ctx = m->cfg.max_ctx;
+  p.eps = m->cfg.rms_eps;
+  p.vw = m->vw;
+  p.vhead = m->vhead;
+  p.layer_bf16 = m->vlayer_bf16;
+  p.head_bf16 = m->vhead_bf16;
+  p.kc = m->kc;
+  p.vc = m->vc;
+  p.rope_cos = m->rope_cos;
+  p.rope_sin = m->rope_sin;
+  p.tokens = tokens_dev;
+  p.k = k;
+  p.pos0 = pos0;
+  p.next_out = next_dev;
+  p.logits = logits_dev;
+  m->vsteps += 1;
+  const size_t w = v_x_words(m->cfg.n_layers);
+  p.x = m->vx + (m->vsteps & 1u) * w;
+  p.x_reset = m->vx + ((m->vsteps + 1u) & 1u) * w;
+  p.sync = m->sync;
+  p.timeout_ns = m->timeout_ns;
+  if (launch_verify(p, m->stream)) return set_err(m, MK_ECUDA, "verify launch: %s", cudaGetErrorString(cudaGetLastError()));
   return MK_OK;
 }
 

@@ -226,12 +226,13 @@ struct Producer {
         while (!mbar_try_wait(&s->empty[slot], par)) {
           if (s->abort) return false;
           if (globaltimer() - t0 > deadline_ns) {  // the consumers stopped releasing slots
+            // recorded in the status words only: the consumers read this CTA's abort flag right
+            // after their barriers and learn of the failure through status word 2
             if (P->sync) {
               if (atomicCAS(&P->sync->status[0], 0u, 3u) == 0u)
                 st_relaxed_u32(&P->sync->status[1], (uint32_t)PH_WAIT | ((uint32_t)blockIdx.x << 16) | 0x80000000u);
               st_relaxed_u32(&P->sync->status[2], 1u);
             }
-            s->abort = 1;
             return false;
           }
         }

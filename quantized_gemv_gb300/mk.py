@@ -57,7 +57,8 @@ class mk_weights(C.Structure):
 EXPORTS = ("mk_max_context", "mk_decode_grid", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
            "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
            "mk_pack_fp8_row", "mk_pack_fp8_row_bf16scale", "mk_pack_nvfp4", "mk_pack_nvfp4_mse", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
-           "mk_decode_step_static")
+           "mk_decode_step_static", "mk_verify_workspace_bytes", "mk_verify_attach", "mk_verify_step")
+MK_VERIFY_MAX = 8
 
 _lib = None
 
@@ -91,6 +92,10 @@ def lib():
         L.mk_gemv.argtypes = [C.POINTER(mk_mat), C.c_int, C.c_int, vp, vp, vp]
         L.mk_stream_read.argtypes = [vp, sz, vp]
         L.mk_probe_cvt.argtypes = [vp, vp, vp, C.c_int, vp, vp, vp]
+        L.mk_verify_workspace_bytes.restype = sz
+        L.mk_verify_workspace_bytes.argtypes = [vp]
+        L.mk_verify_attach.argtypes = [vp, vp, sz]
+        L.mk_verify_step.argtypes = [vp, vp, i32, i32, vp, vp]
         L.mk_decode_step_static.argtypes = [C.POINTER(mk_config), C.POINTER(mk_weights), vp, vp, i32, i32,
                                             C.POINTER(i32), vp, vp]
         _lib = L
@@ -294,6 +299,17 @@ class Model:
         self._err(lib().mk_trace_dump(self.h, buf.ctypes.data_as(C.c_void_p), cap, C.byref(written)), "mk_trace_dump")
         recs = buf[: written.value].view(TRACE_DTYPE)
         return recs.reshape(len(recs) // TRACE_PER_CTA, TRACE_PER_CTA)  # one row of records per CTA of the grid
+
+    def verify_attach(self):
+        """Repack the weights for mk_verify_step into a workspace this object keeps."""
+        n = lib().mk_verify_workspace_bytes(self.h)
+        self.verify_workspace = torch.empty(n, dtype=torch.uint8, device="cuda")
+        self._err(lib().mk_verify_attach(self.h, _ptr(self.verify_workspace), n), "mk_verify_attach")
+
+    def verify_step(self, tokens_dev: torch.Tensor, pos0: int, next_dev: torch.Tensor, logits=None):
+        """One batched verify launch over the k = len(tokens_dev) tokens (int32 CUDA tensors)."""
+        self._err(lib().mk_verify_step(self.h, _ptr(tokens_dev), int(tokens_dev.numel()), int(pos0), _ptr(next_dev),
+                                       _ptr(logits)), "mk_verify_step")
 
     def debug_fault(self, cta: int, phase: int, timeout_ms: int = 0):
         self._err(lib().mk_debug_fault(self.h, cta, phase, timeout_ms), "mk_debug_fault")
