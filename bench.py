@@ -606,7 +606,8 @@ def main():
                                   plain_tok_s=v["runs"]["median_tok_s"] if v else None)
             xr = {"headline": xr, "qwen3_0.6b_fp8_ctx4096": xr_ctx}
     layer1 = run_layer1(mk) if rank == 0 and not args.no_layer1 else None
-    verify = run_verify(mk) if rank == 0 and not args.no_verify else None
+    verify = (run_verify(mk, wl.name if wl.prefill + wl.prompt_len + 8 * 19 <= 1024 else HEADLINE)
+              if rank == 0 and not args.no_verify else None)
     sweep = run_sweep(mk) if rank == 0 and not args.no_sweep else None
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

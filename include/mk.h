@@ -33,6 +33,7 @@ extern "C" {
 #define MK_ETIMEOUT (-3)     /* a device-side wait exceeded its deadline; the step was abandoned */
 #define MK_ENORESIDENT (-4)  /* the persistent grid cannot be made co-resident on this GPU */
 #define MK_ENOTRACE (-5)     /* X-ray requested but the model was created without it */
+#define MK_EBOUNDS (-6)      /* bounds-checking build only: a device access out of range was skipped */
 
 /* ---------------------------------------------------------------- weight formats
  * MK_BF16:    data = bf16 [rows][cols]; scale = NULL.
@@ -170,6 +171,13 @@ int mk_trace_dump(mk_model* m, void* host_buf, size_t cap, size_t* written);
  * that every wait on it runs out; with timeout_ms the device deadline of every wait. Pass
  * cta = -1 to disable. The failed step returns MK_ETIMEOUT and the model stays usable. */
 int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms);
+
+/* Race-detection aid (an addition of this library; the pages have no counterpart): with seed != 0,
+ * every CTA of the following steps waits a pseudo-random 0 .. 20 us (a hash of the seed, the CTA,
+ * the layer and the step, timed with %globaltimer) before each step, so the CTAs reach every
+ * exchange in a different order; a correct step gives bit-identical results. seed = 0 turns it
+ * off. */
+int mk_debug_stress(mk_model* m, uint32_t seed);
 
 /* ---------------------------------------------------------------- building blocks */
 

@@ -38,6 +38,7 @@ struct mk_model {
   uint32_t* host_status;  // pinned: SyncBlock::status and ::tok lines (64 words)
   unsigned long long timeout_ns;
   int fault_cta, fault_phase;
+  uint32_t stress_seed = 0;
   std::string err;
   // batched verify (mk_verify_attach)
   std::vector<DLayer> hlayers;  // host copy of the layer table
@@ -326,6 +327,7 @@ static KParams base_params(mk_model* m) {
   p.timeout_ns = m->timeout_ns;
   p.fault_cta = m->fault_cta;
   p.fault_phase = m->fault_phase;
+  p.stress_seed = m->stress_seed;
   return p;
 }
 
@@ -364,6 +366,16 @@ static int collect_status(mk_model* m, int32_t* next_token) {
     if (m->vx) cudaMemsetAsync(m->vx, 0xFF, 2 * v_x_words(m->cfg.n_layers) * sizeof(uint32_t), m->stream);
     cudaStreamSynchronize(m->stream);
     return MK_EINVAL;
+  }
+  if (st == 5) {
+    const uint32_t d = m->host_status[1];
+    set_err(m, MK_EBOUNDS, "out-of-range device access skipped (bounds-checking build): site %u index %u", d >> 24,
+            d & 0xFFFFFFu);
+    cudaMemsetAsync(m->sync, 0, sizeof(SyncBlock), m->stream);
+    if (m->acc) cudaMemsetAsync(m->acc, 0, 2 * (size_t)m->cfg.n_layers * HID * sizeof(unsigned long long), m->stream);
+    if (m->vx) cudaMemsetAsync(m->vx, 0xFF, 2 * v_x_words(m->cfg.n_layers) * sizeof(uint32_t), m->stream);
+    cudaStreamSynchronize(m->stream);
+    return MK_EBOUNDS;
   }
   if (st != 0) {
     const uint32_t d = m->host_status[1];
@@ -470,6 +482,12 @@ int mk_debug_fault(mk_model* m, int cta, int phase, int timeout_ms) {
   m->fault_cta = cta;
   m->fault_phase = phase;
   if (timeout_ms > 0) m->timeout_ns = (unsigned long long)timeout_ms * 1000000ull;
+  return MK_OK;
+}
+
+int mk_debug_stress(mk_model* m, uint32_t seed) {
+  if (!m) return MK_EINVAL;
+  m->stress_seed = seed;
   return MK_OK;
 }
 

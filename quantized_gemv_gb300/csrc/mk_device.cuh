@@ -136,6 +136,24 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
       : "memory");
 }
 
+// ------------------------------------------------------------------ debug bounds checks
+// Built with MK_DEBUG_BOUNDS (libmk_debug.so), a checked access whose index is out of range is
+// skipped and recorded: status word 0 = 5 (first failure wins), word 1 = site << 24 | low bits of
+// the index, word 2 = 1 (every CTA stops at its next wait). In the normal build the check is
+// compiled away (always true). status: the SyncBlock's status words, or null.
+__device__ __forceinline__ bool mk_in_bounds(bool ok, uint32_t* status, uint32_t site, uint32_t value) {
+#ifdef MK_DEBUG_BOUNDS
+  if (!ok && status) {
+    if (atomicCAS(&status[0], 0u, 5u) == 0u) st_relaxed_u32(&status[1], (site << 24) | (value & 0xFFFFFFu));
+    st_relaxed_u32(&status[2], 1u);
+  }
+  return ok;
+#else
+  (void)ok, (void)status, (void)site, (void)value;
+  return true;
+#endif
+}
+
 // ------------------------------------------------------------------ register dequantisation
 // E4M3 pair (low byte = first element) -> two floats (exact).
 __device__ __forceinline__ float2 e4m3x2_to_f2(uint32_t pair16) {

@@ -107,6 +107,7 @@ struct KParams {
   unsigned long long timeout_ns;
   int fault_cta;         // test hook (-1 = off)
   int fault_phase;
+  uint32_t stress_seed;  // test hook: nonzero = every CTA waits a seeded 0..20 us before each step
   // Folded O-projection (contexts of one attention unit, grid FOLD_GRID): every CTA b runs the
   // attention of q head b / FOLD_SLICES and multiplies its output by the 128 x 128 block of W_o
   // whose rows are [128 (b % FOLD_SLICES), +128) and whose columns are that head's; the partial

@@ -174,10 +174,13 @@ struct Xray {
     base = t ? t + (size_t)blockIdx.x * TRACE_PER_CTA : nullptr;
     n = 0;
   }
+  // Begin stamps (kinds 0 and 2, except the first, the embedding's) record only the SM clock: the
+  // analyser places them on the global timeline from the CTA's neighbouring full stamps, which
+  // halves the costly %globaltimer reads.
   __device__ __forceinline__ void stamp(int phase, int kind) {
     if (XR >= 1 && base && n < TRACE_PER_CTA) {
       TraceRec r;
-      r.gtime = globaltimer();
+      r.gtime = ((kind == 0 || kind == 2) && phase != PH_EMBED) ? 0ull : globaltimer();
       r.clk = clock64_();
       r.smid = smid();
       r.cta = (uint16_t)blockIdx.x;
@@ -362,6 +365,7 @@ struct Consumer {
   float eps;   // RMSNorm epsilon
   Xray<XR> xr;
 
+  __device__ __forceinline__ uint32_t* dbg_status() const { return P->sync ? P->sync->status : nullptr; }
   __device__ void fail(uint32_t code, uint32_t detail) {
     // first failure wins; tell every CTA to stop
     if (P->sync) {
@@ -375,6 +379,20 @@ struct Consumer {
   }
   __device__ __forceinline__ void mark(int id) {  // sub-phase mark (kind 4), X-ray builds only
     if (tid == 0) xr.mark(id);
+  }
+  // Race-detection aid: a pseudo-random wait of 0 .. 20 us (a hash of the seed, this CTA, the layer
+  // and the step) before a step, so the CTAs reach each exchange in a different order every run;
+  // results must not change. Bounded by %globaltimer; off (seed 0) in normal operation.
+  __device__ void stress_delay(uint32_t seed, int layer, int step) const {
+    uint32_t h = seed ^ (blockIdx.x * 0x9E3779B1u) ^ ((uint32_t)layer * 0x85EBCA77u) ^ ((uint32_t)step * 0xC2B2AE3Du);
+    h ^= h >> 16;
+    h *= 0x7FEB352Du;
+    h ^= h >> 15;
+    h *= 0x846CA68Bu;
+    h ^= h >> 16;
+    const uint64_t t0 = globaltimer(), wait_ns = h % 20000u;
+    while (globaltimer() - t0 < wait_ns) {
+    }
   }
   __device__ __forceinline__ bool faulted(int phase, int layer) const {
     return P->fault_cta == (int)blockIdx.x && P->fault_phase == phase && layer == 0;
@@ -565,13 +583,17 @@ struct Consumer {
     auto body = [&](int ch, const float4* x) {
 #pragma unroll
       for (int r = 0; r < NR; ++r) {
-        const uint4 w = *reinterpret_cast<const uint4*>(code[r] + ch * 512 + lane * 16);
+        const uint8_t* wp = code[r] + ch * 512 + lane * 16;
+        if (!mk_in_bounds(wp >= ring && wp + 16 <= ring + RING_BYTES, dbg_status(), 1, (uint32_t)(wp - ring))) wp = ring;
+        const uint4 w = *reinterpret_cast<const uint4*>(wp);
         if constexpr (FMT == 0) {
           dot_bf16_16B(w, x, acc[r]);
         } else if constexpr (FMT == 1) {
           dot_fp8_16B(w, x, acc[r]);
         } else {
-          const float2 bs = e4m3x2_to_f2(*reinterpret_cast<const uint16_t*>(bsc[r] + ch * 64 + lane * 2));
+          const uint8_t* sp = bsc[r] + ch * 64 + lane * 2;
+          if (!mk_in_bounds(sp >= ring && sp + 2 <= ring + RING_BYTES, dbg_status(), 2, (uint32_t)(sp - ring))) sp = ring;
+          const float2 bs = e4m3x2_to_f2(*reinterpret_cast<const uint16_t*>(sp));
           dot_nvfp4_16B(w, x, bs.x, bs.y, acc[r]);
         }
       }
@@ -612,14 +634,14 @@ struct Consumer {
   int besti;
   __device__ __forceinline__ void epi_row(const EpiCtx& e, int r, float y) {
     if (e.kind == EPI_QKV) {
-      if (!e.skip) ll_store(e.ll + r, e.tag, y * e.inv);
+      if (!e.skip && mk_in_bounds(r < QROWS, dbg_status(), 5, (uint32_t)r)) ll_store(e.ll + r, e.tag, y * e.inv);
     } else if (e.kind == EPI_RESID) {
       const float v = s->hs[r] + y;
-      if (!e.skip) ll_store(e.ll + r, e.tag, v);
+      if (!e.skip && mk_in_bounds(r < HID, dbg_status(), 5, (uint32_t)r)) ll_store(e.ll + r, e.tag, v);
       if (e.dbg) e.dbg[r] = v;
     } else if (e.kind == EPI_HEAD) {
       y *= e.inv;
-      if (e.fout) e.fout[r] = y;
+      if (e.fout && mk_in_bounds(r < P->vocab, dbg_status(), 6, (uint32_t)r)) e.fout[r] = y;
       if (y > best || (y == best && r < besti)) {
         best = y;
         besti = r;
@@ -847,7 +869,8 @@ struct Consumer {
             if (lane == k / 2) g = part[k] * sc[k], up = part[k + 1] * sc[k + 1];
           if (lane < UPG && g0 + lane < nrows) {
             g *= e.inv, up *= e.inv;
-            if (!e.skip) ll_store(e.ll + g0 + lane, e.tag, g / (1.0f + expf(-g)) * up);
+            if (!e.skip && mk_in_bounds(r0 + g0 + lane < FFN, dbg_status(), 5, (uint32_t)(r0 + g0 + lane)))
+              ll_store(e.ll + g0 + lane, e.tag, g / (1.0f + expf(-g)) * up);
           }
         } else {
           float y = part[0] * sc[0];
@@ -933,7 +956,8 @@ struct Consumer {
       if (c == 0 && !skip) {
         const float sc = FMT == 1 ? __ldg(reinterpret_cast<const float*>(mo.scale) + r0 + r) : (FMT == 2 ? mo.tscale : 1.f);
         const long long f = __float2ll_rn(v * sc * COUNT_SCALE);
-        red_add_u64(p.acc + (size_t)l * HID + r0 + r, ((unsigned long long)f << 8) + 1ull);
+        if (mk_in_bounds(l < p.n_layers && r0 + r < HID, dbg_status(), 7, (uint32_t)(r0 + r)))
+          red_add_u64(p.acc + (size_t)l * HID + r0 + r, ((unsigned long long)f << 8) + 1ull);
       }
     }
   }
@@ -1017,7 +1041,7 @@ struct Consumer {
         for (int j = 0; j < 4; ++j) {
           const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
           v[j] = bf16f(bits);
-          if (S.kvw) cache[row + lane + 32 * j] = bits;
+          if (S.kvw && mk_in_bounds(p.pos < p.max_ctx, dbg_status(), 3, (uint32_t)p.pos)) cache[row + lane + 32 * j] = bits;
           (warp == 2 ? s->knew : s->vnew)[lane + 32 * j] = bits;
         }
       }
@@ -1045,7 +1069,10 @@ struct Consumer {
     // and P.V over it (flash-decoding within the CTA); one CTA barrier merges the eight partials.
     const int per = (np + NCW - 1) / NCW;
     const int ws0 = min(np, warp * per), ws1 = min(np, ws0 + per);
-    auto tile_of = [&](int t) { return ring + (size_t)((n + (t >> 5)) % NSLOT) * SLOT + (t & (KVT - 1)) * (HD * 2); };
+    auto tile_of = [&](int t) {
+      const int tl = mk_in_bounds((t >> 5) < ntiles, dbg_status(), 4, (uint32_t)t) ? (t >> 5) : 0;
+      return ring + (size_t)((n + tl) % NSLOT) * SLOT + (t & (KVT - 1)) * (HD * 2);
+    };
     // ---- scores: four lanes per position, 32 dimensions per lane as four 16-byte chunks; odd
     // positions start at the other half of the banks, so a quarter warp reads two rows without
     // conflicts, and each lane keeps the matching q elements of both heads in registers
@@ -1277,6 +1304,7 @@ struct Consumer {
       const uint32_t tag = p.tagbase + (uint32_t)l;
       for (int step = head ? ST_HEAD : ST_QKV; step <= (head ? ST_HEAD : ST_DOWN); ++step) {
         mark(59);
+        if (p.stress_seed) stress_delay(p.stress_seed, l, step);
         if (step == ST_ATTN) {
           if (S.unit) {
             st(PH_ATTN, 0);

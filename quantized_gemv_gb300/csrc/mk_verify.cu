@@ -115,7 +115,8 @@ int launch_verify_repack_head(const DMat& e, int vocab, int to_bf16, uint8_t* ds
 // ------------------------------------------------------------------ kernel layout
 constexpr int V_RING = V_NSLOT * SLOT;         // weight ring (96 KB)
 constexpr int V_XB = (FFN / 64) * VN * 128;    // B operand for K up to FFN: 48 boxes x 16 rows x 128 B
-constexpr uint32_t V_TMEM_COLS = 32;           // D: 128 lanes x 16 fp32 columns (32 allocated)
+constexpr int V_NACC = 4;                      // accumulators: box j adds into accumulator j % V_NACC
+constexpr uint32_t V_TMEM_COLS = 64;           // D: 128 lanes x V_NACC x 16 fp32 columns
 
 struct __align__(16) VSmem {
   uint64_t full[V_NSLOT];
@@ -367,8 +368,10 @@ struct VCons {
           L.x = lo[0] | ((uint32_t)lo[1] << 16), L.y = lo[2] | ((uint32_t)lo[3] << 16);
           L.z = lo[4] | ((uint32_t)lo[5] << 16), L.w = lo[6] | ((uint32_t)lo[7] << 16);
           uint8_t* box = xb + (size_t)(e0 / 64) * (VN * 128);
-          *reinterpret_cast<uint4*>(box + sw128_offset(t, (e0 % 64) / 8)) = H;
-          *reinterpret_cast<uint4*>(box + sw128_offset(8 + t, (e0 % 64) / 8)) = L;
+          if (mk_in_bounds((e0 / 64 + 1) * VN * 128 <= V_XB && t < VK, p.sync->status, 11, (uint32_t)e0)) {
+            *reinterpret_cast<uint4*>(box + sw128_offset(t, (e0 % 64) / 8)) = H;
+            *reinterpret_cast<uint4*>(box + sw128_offset(8 + t, (e0 % 64) / 8)) = L;
+          }
           if (w) {  // a warp's 32 chunks of a round belong to one token (cpt is a multiple of 32)
 #pragma unroll
             for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
@@ -403,11 +406,18 @@ struct VCons {
           break;
         }
         const uint32_t sbase = smem_u32(ring + (size_t)slot * SLOT);
+        // the MMA reads 128 rows (16 KB) from a box's start; they end inside the ring and xb
+        if (!mk_in_bounds(slot < V_NSLOT && (slot + 1) * SLOT + (g.bps - 1) * g.R8 * 128 <= V_RING + V_XB - 16384 + SLOT,
+                          p.sync->status, 14, slot))
+          break;
+        // consecutive boxes go to different accumulators, so their MMAs do not wait on one another
         for (int b = 0; b < g.bps && j < g.nbox; ++b, ++j) {
+          const uint32_t d = s->tmem + (uint32_t)((j % V_NACC) * VN);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_f16(s->tmem, umma_desc_sw128(sbase + (uint32_t)(b * g.R8 * 128 + 32 * kk)),
-                     umma_desc_sw128(xbase + (uint32_t)(j * VN * 128 + 32 * kk)), idesc, (j | kk) != 0 ? 1u : 0u);
+            umma_f16(d, umma_desc_sw128(sbase + (uint32_t)(b * g.R8 * 128 + 32 * kk)),
+                     umma_desc_sw128(xbase + (uint32_t)(j * VN * 128 + 32 * kk)), idesc,
+                     (j >= V_NACC || kk != 0) ? 1u : 0u);
         }
         umma_commit(&s->empty[slot]);
       }
@@ -421,12 +431,18 @@ struct VCons {
     bar_consumers(NCT);  // every consumer thread is past its writes of the abort flag
     return s->abort == 0;
   }
-  // This thread's accumulator row (warps 0..3: tensor-memory lane 32 warp + lane): y[t] for t < k.
+  // This thread's accumulator row (warps 0..3: tensor-memory lane 32 warp + lane): y[t] for t < k,
+  // the accumulators and the high and low parts summed in a fixed order.
   __device__ void read_rows(float* y) {
-    float d[16];
-    tmem_ld16(s->tmem + ((uint32_t)(32 * (warp & 3)) << 16), d);
 #pragma unroll
-    for (int t = 0; t < VK; ++t) y[t] = d[t] + d[8 + t];
+    for (int t = 0; t < VK; ++t) y[t] = 0.f;
+#pragma unroll
+    for (int a = 0; a < V_NACC; ++a) {
+      float d[16];
+      tmem_ld16(s->tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a * VN), d);
+#pragma unroll
+      for (int t = 0; t < VK; ++t) y[t] += d[t] + d[8 + t];
+    }
     tc_fence_before();
   }
   // Row scale of a canonical matrix after the 16-bit GEMM: FP8 row scale, NVFP4 tensor scale, 1.
@@ -498,7 +514,8 @@ __device__ bool v_attention(VCons& C, int l) {
       for (int j = 0; j < 4; ++j) {
         const uint16_t bits = __bfloat16_as_ushort(__float2bfloat16_rn(v[j]));
         dst[lane + 32 * j] = bits;
-        if (h % GQA == 0 && tok == t) cache[row + lane + 32 * j] = bits;
+        if (h % GQA == 0 && tok == t && mk_in_bounds(p.pos0 + tok < p.max_ctx, p.sync->status, 13, (uint32_t)tok))
+          cache[row + lane + 32 * j] = bits;
       }
     }
   }
@@ -538,7 +555,7 @@ __device__ bool v_attention(VCons& C, int l) {
     }
 #pragma unroll
     for (int o = 4; o; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
-    if (pp < ws1) {
+    if (pp < ws1 && mk_in_bounds(pp < V_MAXPOS, p.sync->status, 12, (uint32_t)pp)) {
       a *= scale;
       if (sl == 0) s->sc[pp] = a;
       m = fmaxf(m, a);

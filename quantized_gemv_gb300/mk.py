@@ -15,12 +15,12 @@ import torch
 from . import build as _build
 from .synthetic import FMT_BF16, FMT_FP8_ROW, FMT_NVFP4, LINEARS, ModelConfig
 
-MK_OK, MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, MK_ENOTRACE = 0, -1, -2, -3, -4, -5
+MK_OK, MK_EINVAL, MK_ECUDA, MK_ETIMEOUT, MK_ENORESIDENT, MK_ENOTRACE, MK_EBOUNDS = 0, -1, -2, -3, -4, -5, -6
 MK_FLAG_XRAY = 1
 MK_FLAG_XRAY_MARKS = 4
 MK_FLAG_NO_FOLD = 8
 ERRNAMES = {MK_EINVAL: "MK_EINVAL", MK_ECUDA: "MK_ECUDA", MK_ETIMEOUT: "MK_ETIMEOUT",
-            MK_ENORESIDENT: "MK_ENORESIDENT", MK_ENOTRACE: "MK_ENOTRACE"}
+            MK_ENORESIDENT: "MK_ENORESIDENT", MK_ENOTRACE: "MK_ENOTRACE", MK_EBOUNDS: "MK_EBOUNDS"}
 TRACE_DTYPE = np.dtype([("gtime", "<u8"), ("clk", "<u8"), ("smid", "<u4"), ("cta", "<u2"),
                         ("phase", "u1"), ("kind", "u1")])
 TRACE_PER_CTA = 2048  # records kept per CTA (the kernel's trace row length)
@@ -57,16 +57,18 @@ class mk_weights(C.Structure):
 EXPORTS = ("mk_max_context", "mk_decode_grid", "mk_workspace_bytes", "mk_create", "mk_destroy", "mk_last_error", "mk_decode_step",
            "mk_decode_greedy", "mk_decode_next", "mk_sync", "mk_kv_cache", "mk_debug_hidden", "mk_trace_dump", "mk_debug_fault",
            "mk_pack_fp8_row", "mk_pack_fp8_row_bf16scale", "mk_pack_nvfp4", "mk_pack_nvfp4_mse", "mk_gemv", "mk_stream_read", "mk_probe_cvt",
-           "mk_decode_step_static", "mk_verify_workspace_bytes", "mk_verify_attach", "mk_verify_step")
+           "mk_decode_step_static", "mk_debug_stress", "mk_verify_workspace_bytes", "mk_verify_attach", "mk_verify_step")
 MK_VERIFY_MAX = 8
 
 _lib = None
 
 
 def lib():
+    """The library, built if needed: libmk.so, or the bounds-checking libmk_debug.so when the
+    environment variable MK_LIBRARY is "debug" (checked once, at the first call)."""
     global _lib
     if _lib is None:
-        path = _build.build()
+        path = _build.build(debug=os.environ.get("MK_LIBRARY", "") == "debug")
         L = C.CDLL(path)
         vp, i32, sz = C.c_void_p, C.c_int32, C.c_size_t
         L.mk_max_context.restype = C.c_int
@@ -85,6 +87,7 @@ def lib():
         L.mk_debug_hidden.argtypes = [vp, vp]
         L.mk_trace_dump.argtypes = [vp, vp, sz, C.POINTER(sz)]
         L.mk_debug_fault.argtypes = [vp, C.c_int, C.c_int, C.c_int]
+        L.mk_debug_stress.argtypes = [vp, C.c_uint32]
         L.mk_pack_fp8_row.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp]
         L.mk_pack_fp8_row_bf16scale.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp]
         L.mk_pack_nvfp4.argtypes = [vp, C.c_int, C.c_int, vp, vp, vp, vp]
@@ -299,6 +302,10 @@ class Model:
         self._err(lib().mk_trace_dump(self.h, buf.ctypes.data_as(C.c_void_p), cap, C.byref(written)), "mk_trace_dump")
         recs = buf[: written.value].view(TRACE_DTYPE)
         return recs.reshape(len(recs) // TRACE_PER_CTA, TRACE_PER_CTA)  # one row of records per CTA of the grid
+
+    def debug_stress(self, seed: int):
+        """Seeded 0..20 us per-CTA waits before every step (0 = off); results must not change."""
+        self._err(lib().mk_debug_stress(self.h, int(seed)), "mk_debug_stress")
 
     def verify_attach(self):
         """Repack the weights for mk_verify_step into a workspace this object keeps."""

@@ -25,18 +25,27 @@ KIND_BEGIN, KIND_END, KIND_WAIT_BEGIN, KIND_WAIT_END, KIND_MARK, KIND_STOP = 0, 
 
 def records(trace: np.ndarray):
     """Yield (cta, [(t_ns, phase, kind), ...]) for every CTA that wrote records (phase and wait
-    stamps; sub-phase marks, which carry only the SM clock, are left out)."""
+    stamps; sub-phase marks, which carry only the SM clock, are left out).
+
+    Begin stamps (phase and wait begins) carry only the SM clock (their %globaltimer field is 0):
+    their global time is interpolated linearly in clock64 between the CTA's neighbouring stamps
+    that carry both, which is exact while the SM clock holds still between them."""
     for cta in range(trace.shape[0]):
         rows = trace[cta]
-        out = []
-        for r in rows:
-            if r["kind"] == KIND_STOP or (r["gtime"] == 0 and r["kind"] == 0 and r["phase"] == 0):
-                break
-            if r["kind"] == KIND_MARK:
-                continue
-            out.append((int(r["gtime"]), int(r["phase"]), int(r["kind"])))
-        if out:
-            yield cta, out
+        ends = np.flatnonzero((rows["kind"] == KIND_STOP) | ((rows["gtime"] == 0) & (rows["clk"] == 0)))
+        rs = rows[: ends[0]] if len(ends) else rows
+        rs = rs[rs["kind"] != KIND_MARK]
+        if len(rs) == 0:
+            continue
+        g = rs["gtime"].astype(np.float64)
+        c = rs["clk"].astype(np.float64)
+        full = g != 0
+        if full.any() and not full.all():
+            if full.sum() >= 2:
+                g[~full] = np.interp(c[~full], c[full], g[full])
+            else:
+                g[~full] = g[full][0]
+        yield cta, [(int(round(t)), int(ph), int(k)) for t, ph, k in zip(g, rs["phase"], rs["kind"])]
 
 
 def analyze(trace: np.ndarray, bytes_by_phase: dict | None = None) -> dict:

@@ -140,3 +140,33 @@ def test_folded_o_projection_matches_unfolded(variant):
     assert worst <= 1e-3, worst
     fold.close()
     plain.close()
+
+
+@pytest.mark.parametrize("variant", ["bf16", "nvfp4"])
+def test_stress_delays_change_nothing(variant):
+    """Seeded per-CTA waits before every step reorder the CTAs' arrivals at every exchange (and at
+    the folded O-projection's accumulators); tokens, logits and hidden states stay bit-identical,
+    at short contexts and at one past the single-unit attention window."""
+    cfg = S.ModelConfig(n_layers=2, vocab=4099, max_ctx=512)
+    _, model, _ = make_pair(cfg, variant, seed=87)
+    toks = S.prompt_ids(cfg, 300, seed=12)
+    checked = (3, 40, 288, 290)
+
+    def run(seed):
+        model.debug_stress(seed)
+        out = []
+        for pos in range(max(checked) + 1):
+            lg = torch.empty(cfg.vocab, dtype=torch.float32, device="cuda")
+            nxt = model.decode_step(int(toks[pos]), pos, lg)
+            if pos in checked:
+                out.append((nxt, lg.cpu().numpy().copy(), model.hidden().cpu().numpy().copy()))
+        return out
+
+    ref = run(0)
+    for seed in (1, 2):
+        for a, b in zip(ref, run(seed)):
+            assert a[0] == b[0]
+            assert np.array_equal(a[1].view(np.uint32), b[1].view(np.uint32))
+            assert np.array_equal(a[2].view(np.uint32), b[2].view(np.uint32))
+    model.debug_stress(0)
+    model.close()

@@ -12,11 +12,14 @@ B, E, WB, WE, MARK, STOP = 0, 1, 2, 3, 4, 255
 QKV, ATT, O, GU, DOWN, HEAD, EMBED = 0, 1, 2, 3, 4, 5, 6
 
 
-def _trace(rows_per_cta, width=64):
+def _trace(rows_per_cta, width=64, clock_only_begins=False):
+    """Records {t, clk = 7 t + 1}; with clock_only_begins, phase and wait begins keep only the
+    clock (gtime 0), as the kernel writes them after the embedding's first stamp."""
     tr = np.zeros((len(rows_per_cta), width), dtype=TRACE_DTYPE)
     for c, rows in enumerate(rows_per_cta):
         for i, (t, ph, kind) in enumerate(rows + [(0, 0, STOP)]):
-            tr[c][i] = (t, 7 * t, 3, c, ph, kind)
+            g = 0 if (clock_only_begins and kind in (B, WB) and ph != EMBED) else t
+            tr[c][i] = (g, 7 * t + 1, 3, c, ph, kind)
     return tr
 
 
@@ -49,6 +52,17 @@ def test_analyze_hand_trace():
     # idle: a ends last (1500); b ends at 1480
     assert r["idle_ns"] == pytest.approx(10)
     assert xray.layer_timeline(tr) == []  # one layer: no layer-to-layer interval
+
+
+def test_clock_only_begin_stamps_are_placed_by_interpolation():
+    a = [(1000, EMBED, B), (1010, EMBED, E)] + _one_layer(1010, 40) + [(1350, DOWN, WB), (1360, DOWN, WE),
+                                                                       (1360, HEAD, B), (1500, HEAD, E)]
+    b = [(1005, EMBED, B), (1012, EMBED, E)] + _one_layer(1012, 20) + [(1332, DOWN, WB), (1340, DOWN, WE),
+                                                                       (1340, HEAD, B), (1480, HEAD, E)]
+    full, sparse = _trace([a, b]), _trace([a, b], clock_only_begins=True)
+    assert (sparse["gtime"] == 0).sum() > (full["gtime"] == 0).sum()
+    assert dict(xray.records(full)) == dict(xray.records(sparse))
+    assert xray.analyze(full) == xray.analyze(sparse)
 
 
 @pytest.mark.gpu
