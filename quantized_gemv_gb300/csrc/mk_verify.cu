@@ -38,43 +38,49 @@ __device__ uint16_t v_elem(const DMat& m, int K, int row, int col) {
   return __half_as_ushort(__float2half_rn(v));
 }
 
-// Block (step s, CTA c) of one layer: rows of the source matrices for block row r (-1: padding).
+// Row r (0 .. R - 1) of CTA c's rows of step s: the source matrix (which) and its row.
 __device__ int v_src_row(int s, int c, int r, int& which) {
-  which = 0;
   if (s == VS_QKV) {  // q rows to CTAs 0..63, k rows to 64..95, v rows to 96..127, 32 each
     which = c < 64 ? M_Q : (c < 96 ? M_K : M_V);
     const int base = c < 64 ? c : (c < 96 ? c - 64 : c - 96);
     return 32 * base + r;
   }
-  if (s == VS_GU) {  // 24 gate rows then the same 24 up rows
-    which = r < 24 ? M_GATE : M_UP;
-    return 24 * c + (r % 24);
+  if (s == VS_GU) {  // 32 gate rows then the same 32 units' up rows
+    which = r < 32 ? M_GATE : M_UP;
+    return 32 * c + (r % 32);
   }
   which = s == VS_O ? M_O : M_DOWN;
   return 8 * c + r;
 }
 
-// bf16 matrices are copied bit for bit; FP8 and NVFP4 ones become f16 (to_bf16 = 0).
+// One block (layer step s, CTA c): box b, tile row L = seg * R + r, 16-byte chunk cc holds row r's
+// inputs seg * KS + 64 b + 8 cc .. + 7. bf16 matrices are copied bit for bit; FP8 and NVFP4 ones
+// become f16 (to_bf16 = 0).
 __global__ void k_verify_repack_layer(const DLayer L, int to_bf16, uint8_t* __restrict__ dst) {
   (void)to_bf16;
   const int s = blockIdx.y, c = blockIdx.x;
-  const int R8 = v_rows8(s), K = v_cols(s);
-  uint8_t* blk = dst + v_step_offset(s) + (size_t)c * v_block_bytes(s);
-  const int nchunk = R8 * K / 8;  // 16-byte chunks of the block
+  const int nbox = v_nbox(s, c);
+  if (nbox == 0) return;
+  const VStepGeom g = v_step_geom(s);
+  const int K = v_cols(s);
+  uint8_t* blk = dst + v_block_offset(s, c);
+  const int nchunk = nbox * 128 * 8;  // 16-byte chunks of the block
   for (int i = threadIdx.x; i < nchunk; i += blockDim.x) {
-    const int j = i / (R8 * 8), rem = i % (R8 * 8), r = rem / 8, cc = rem % 8;
+    const int bx = i / 1024, rem = i % 1024, tr = rem / 8, cc = rem % 8;
+    const int seg = tr / g.R, r = tr % g.R;
     int which;
     const int row = v_src_row(s, c, r, which);
     const DMat& m = L.m[which];
+    const int col0 = seg * g.KS + 64 * bx + 8 * cc;
     uint16_t v[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = v_elem(m, K, row, 64 * j + 8 * cc + e);
+    for (int e = 0; e < 8; ++e) v[e] = v_elem(m, K, row, col0 + e);
     uint4 w;
     w.x = v[0] | ((uint32_t)v[1] << 16);
     w.y = v[2] | ((uint32_t)v[3] << 16);
     w.z = v[4] | ((uint32_t)v[5] << 16);
     w.w = v[6] | ((uint32_t)v[7] << 16);
-    *reinterpret_cast<uint4*>(blk + (size_t)j * R8 * 128 + sw128_offset(r, cc)) = w;
+    *reinterpret_cast<uint4*>(blk + (size_t)bx * V_BOX + sw128_offset(tr, cc)) = w;
   }
 }
 
@@ -113,10 +119,15 @@ int launch_verify_repack_head(const DMat& e, int vocab, int to_bf16, uint8_t* ds
 }
 
 // ------------------------------------------------------------------ kernel layout
-constexpr int V_RING = V_NSLOT * SLOT;         // weight ring (96 KB)
-constexpr int V_XB = (FFN / 64) * VN * 128;    // B operand for K up to FFN: 48 boxes x 16 rows x 128 B
-constexpr int V_NACC = 4;                      // accumulators: box j adds into accumulator j % V_NACC
-constexpr uint32_t V_TMEM_COLS = 64;           // D: 128 lanes x V_NACC x 16 fp32 columns
+constexpr int V_RING = V_NSLOT * SLOT;  // weight ring (96 KB)
+// B operand: KB boxes of N rows x 128 bytes; the largest is down_proj's (3 x 256 rows, 96 KB), the
+// LM head's is 16 x 16 rows
+__host__ __device__ constexpr int v_xb_bytes(int kb, int n) { return kb * n * 128; }
+constexpr int V_XB = v_xb_bytes(3, 256);
+static_assert(v_xb_bytes(4, 64) <= V_XB && v_xb_bytes(2, 256) <= V_XB && v_xb_bytes(8, 32) <= V_XB &&
+                  v_xb_bytes(HID / 64, VN) <= V_XB,
+              "a step's B operand exceeds the staging buffer");
+constexpr uint32_t V_TMEM_COLS = 256;  // D: 128 lanes x N (<= 256) fp32 columns
 
 struct __align__(16) VSmem {
   uint64_t full[V_NSLOT];
@@ -129,7 +140,8 @@ struct __align__(16) VSmem {
   float inv[VK];            // per-token RMSNorm factors
   float hres[VK][8];        // this CTA's rows of the layer input (o_proj's residual)
   float hres2[VK][8];       // this CTA's rows of h_attn (down_proj's residual)
-  float gu[VK][48];         // gate and up outputs before SwiGLU
+  float gu[VK][64];         // gate and up outputs before SwiGLU
+  float part[128][VK];      // per-segment partial sums of an epilogue (tile row seg * R + r)
   float q[HD];              // attention: the unit's normalised, rotated query
   __align__(16) uint16_t knew[VK][HD];  // keys and values of the new positions (bf16, as cached)
   __align__(16) uint16_t vnew[VK][HD];
@@ -215,10 +227,8 @@ __device__ void v_producer(const VParams& p, VSmem* s, uint8_t* ring) {
   bool ok = true;
   for (int l = 0; l < p.n_layers && ok; ++l) {
     for (int st = 0; st < VS_COUNT && ok; ++st) {
-      const VGeom g = v_geom(v_rows8(st), v_cols(st));
-      const uint8_t* blk = p.vw + (size_t)l * v_layer_bytes() + v_step_offset(st) + (size_t)c * v_block_bytes(st);
-      for (int j = 0; j < g.nbox && ok; j += g.bps)
-        ok = issue(blk + (size_t)j * g.R8 * 128, (uint32_t)(min(g.bps, g.nbox - j) * g.R8 * 128));
+      const uint8_t* blk = p.vw + (size_t)l * v_layer_bytes() + v_block_offset(st, c);
+      for (int j = 0; j < v_nbox(st, c) && ok; ++j) ok = issue(blk + (size_t)j * V_BOX, (uint32_t)V_BOX);
     }
   }
   const int v0 = (int)((long long)p.vocab * c / V_GRID), v1 = (int)((long long)p.vocab * (c + 1) / V_GRID);
@@ -265,13 +275,14 @@ struct VCons {
   uint32_t n;      // ring slots consumed (the MMA issuer's count)
   uint32_t ndone;  // GEMM steps completed (parity of `done`)
 
-  // Stage the k input vectors of a GEMM step into the B operand (token t: high part in row t, low
-  // part in row 8 + t). The inputs are the sentinel words at vx(l, t) + xoff (embed: the embedding
-  // rows of the tokens instead); w (normed inputs, K == HID): the bf16 norm weights, multiplied in,
-  // and each token's sum of squares left in red[t][0..3]; res (optional): elements
-  // [8 res_chunk, +8) of each token saved un-normed.
+  // Stage the k input vectors of a GEMM step into the B operand of a step with segments of KS inputs
+  // and N rows: input e of token t, in segment seg = e / KS, goes to box (e % KS) / 64, high part in
+  // row 16 seg + t, low part in row 16 seg + 8 + t. The inputs are the sentinel words at
+  // vx(l, t) + xoff (embed: the embedding rows of the tokens instead); w (normed inputs,
+  // K == HID): the bf16 norm weights, multiplied in, and each token's sum of squares left in
+  // red[t][0..3]; res (optional): elements [8 res_chunk, +8) of each token saved un-normed.
   __device__ void stage(int l, int xoff, int K, const uint16_t* w, float (*res)[8], int res_chunk, int ab_bf16,
-                        bool embed) {
+                        bool embed, int KS, int N) {
     const VParams& p = *P;
     const int cpt = K / 8, total = p.k * cpt;  // 8-element chunks per token, in all
     constexpr int BATCH = 4;
@@ -367,10 +378,12 @@ struct VCons {
           H.z = hi[4] | ((uint32_t)hi[5] << 16), H.w = hi[6] | ((uint32_t)hi[7] << 16);
           L.x = lo[0] | ((uint32_t)lo[1] << 16), L.y = lo[2] | ((uint32_t)lo[3] << 16);
           L.z = lo[4] | ((uint32_t)lo[5] << 16), L.w = lo[6] | ((uint32_t)lo[7] << 16);
-          uint8_t* box = xb + (size_t)(e0 / 64) * (VN * 128);
-          if (mk_in_bounds((e0 / 64 + 1) * VN * 128 <= V_XB && t < VK, p.sync->status, 11, (uint32_t)e0)) {
-            *reinterpret_cast<uint4*>(box + sw128_offset(t, (e0 % 64) / 8)) = H;
-            *reinterpret_cast<uint4*>(box + sw128_offset(8 + t, (e0 % 64) / 8)) = L;
+          const int seg = e0 / KS, j = e0 - seg * KS, n0 = VN * seg;
+          uint8_t* box = xb + (size_t)(j / 64) * (N * 128);
+          if (mk_in_bounds((j / 64 + 1) * N * 128 <= V_XB && n0 + VN <= N && t < VK, p.sync->status, 11,
+                           (uint32_t)e0)) {
+            *reinterpret_cast<uint4*>(box + sw128_offset(n0 + t, (j % 64) / 8)) = H;
+            *reinterpret_cast<uint4*>(box + sw128_offset(n0 + 8 + t, (j % 64) / 8)) = L;
           }
           if (w) {  // a warp's 32 chunks of a round belong to one token (cpt is a multiple of 32)
 #pragma unroll
@@ -388,10 +401,11 @@ struct VCons {
     return rsqrtf(tot * (1.0f / (float)HID) + P->eps);
   }
 
-  // The MMAs of one GEMM step: D[row][n] = sum over the step's boxes of A (ring slots) x B (xb).
-  // Thread 0 issues them slot by slot, each slot committed to its empty barrier, and finally
-  // commits `done`; every thread then waits for `done`. Returns false after an abort.
-  __device__ bool mma_step(VGeom g, uint32_t idesc, int phase, int layer) {
+  // The MMAs of one GEMM step: D[row][n] = sum over the step's boxes of A (ring slots) x B (xb, boxes
+  // of N rows), one accumulator. Thread 0 issues them slot by slot, each slot committed to its
+  // empty barrier, and finally commits `done`; every thread then waits for `done`. Returns false
+  // after an abort.
+  __device__ bool mma_step(VGeom g, int N, uint32_t idesc, int phase, int layer) {
     const VParams& p = *P;
     bar_consumers(NCT);  // the staged operand and the previous step's tensor-memory reads
     if (tid == 0) {
@@ -406,18 +420,17 @@ struct VCons {
           break;
         }
         const uint32_t sbase = smem_u32(ring + (size_t)slot * SLOT);
-        // the MMA reads 128 rows (16 KB) from a box's start; they end inside the ring and xb
-        if (!mk_in_bounds(slot < V_NSLOT && (slot + 1) * SLOT + (g.bps - 1) * g.R8 * 128 <= V_RING + V_XB - 16384 + SLOT,
+        // the MMA reads 128 rows (16 KB) from a box's start, which end inside the ring and xb, and
+        // N rows of each B box
+        if (!mk_in_bounds(slot < V_NSLOT && (slot + 1) * SLOT + (g.bps - 1) * g.R8 * 128 <= V_RING + V_XB - 16384 + SLOT &&
+                              (min(g.nbox, j + g.bps)) * N * 128 <= V_XB,
                           p.sync->status, 14, slot))
           break;
-        // consecutive boxes go to different accumulators, so their MMAs do not wait on one another
         for (int b = 0; b < g.bps && j < g.nbox; ++b, ++j) {
-          const uint32_t d = s->tmem + (uint32_t)((j % V_NACC) * VN);
 #pragma unroll
           for (int kk = 0; kk < 4; ++kk)
-            umma_f16(d, umma_desc_sw128(sbase + (uint32_t)(b * g.R8 * 128 + 32 * kk)),
-                     umma_desc_sw128(xbase + (uint32_t)(j * VN * 128 + 32 * kk)), idesc,
-                     (j >= V_NACC || kk != 0) ? 1u : 0u);
+            umma_f16(s->tmem, umma_desc_sw128(sbase + (uint32_t)(b * g.R8 * 128 + 32 * kk)),
+                     umma_desc_sw128(xbase + (uint32_t)(j * N * 128 + 32 * kk)), idesc, (j > 0 || kk != 0) ? 1u : 0u);
         }
         umma_commit(&s->empty[slot]);
       }
@@ -431,19 +444,40 @@ struct VCons {
     bar_consumers(NCT);  // every consumer thread is past its writes of the abort flag
     return s->abort == 0;
   }
-  // This thread's accumulator row (warps 0..3: tensor-memory lane 32 warp + lane): y[t] for t < k,
-  // the accumulators and the high and low parts summed in a fixed order.
-  __device__ void read_rows(float* y) {
+  // This thread's accumulator row (warps 0..3: tensor-memory lane L = 32 warp + lane, tile row
+  // seg * R + r with seg = L / R) on its own segment's diagonal block: y[t] = D[L][16 seg + t] +
+  // D[L][16 seg + 8 + t] (high and low parts). A warp's lanes may lie in several segments (R < 32):
+  // the warp loads each of their column blocks and every lane keeps its own.
+  __device__ void read_seg(int R, float* y) {
+    const int L = 32 * warp + lane, seg = L / R;
+    const int s0 = (32 * warp) / R, s1 = (32 * warp + 31) / R;
+    float d[16];
 #pragma unroll
-    for (int t = 0; t < VK; ++t) y[t] = 0.f;
+    for (int i = 0; i < 16; ++i) d[i] = 0.f;
+    for (int sg = s0; sg <= s1; ++sg) {  // warp-uniform
+      float v[16];
+      tmem_ld16(s->tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(VN * sg), v);
+      if (sg == seg) {
 #pragma unroll
-    for (int a = 0; a < V_NACC; ++a) {
-      float d[16];
-      tmem_ld16(s->tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(a * VN), d);
-#pragma unroll
-      for (int t = 0; t < VK; ++t) y[t] += d[t] + d[8 + t];
+        for (int i = 0; i < 16; ++i) d[i] = v[i];
+      }
     }
+#pragma unroll
+    for (int t = 0; t < VK; ++t) y[t] = d[t] + d[8 + t];
     tc_fence_before();
+  }
+  // Warps 0..3: this thread's diagonal-block row into part[L] (see read_seg).
+  __device__ void read_part(int R) {
+    float y[VK];
+    read_seg(R, y);
+#pragma unroll
+    for (int t = 0; t < VK; ++t) s->part[32 * warp + lane][t] = y[t];
+  }
+  // Row r's result for token t: its segments' partial sums added in segment order.
+  __device__ __forceinline__ float seg_sum(int R, int S, int r, int t) const {
+    float a = s->part[r][t];
+    for (int sg = 1; sg < S; ++sg) a += s->part[sg * R + r][t];
+    return a;
   }
   // Row scale of a canonical matrix after the 16-bit GEMM: FP8 row scale, NVFP4 tensor scale, 1.
   __device__ __forceinline__ float row_scale(const DMat& m, int row) const {
@@ -620,67 +654,72 @@ __device__ void v_run(VCons& C) {
       return;
     }
   }
-  const uint32_t id_l = umma_idesc_f16(p.layer_bf16, VN), id_h = umma_idesc_f16(p.head_bf16, VN);
-  const bool epi = warp < 4;       // warps 0..3 read the accumulator (tensor-memory lane quarters)
+  const VStepGeom gq = v_step_geom(VS_QKV), go = v_step_geom(VS_O), gg = v_step_geom(VS_GU), gd = v_step_geom(VS_DOWN);
+  const uint32_t id_q = umma_idesc_f16(p.layer_bf16, gq.N), id_o = umma_idesc_f16(p.layer_bf16, go.N);
+  const uint32_t id_g = umma_idesc_f16(p.layer_bf16, gg.N), id_d = umma_idesc_f16(p.layer_bf16, gd.N);
+  const uint32_t id_h = umma_idesc_f16(p.head_bf16, VN);
+  const bool epi = warp < 4;         // warps 0..3 read the accumulator (tensor-memory lane quarters)
   const int row = 32 * warp + lane;  // this thread's accumulator row
+  const bool gu_cta = c < V_GU_CTAS;
   float y[VK];
   for (int l = 0; l < p.n_layers; ++l) {
     const DLayer& L = p.layers[l];
     // ---- q|k|v: this CTA's 32 rows (CTA c writes q|k|v elements 32 c .. 32 c + 31)
-    C.stage(l == 0 ? 0 : l - 1, VX_H, HID, L.ln_in, s->hres, c, p.layer_bf16, l == 0);
-    if (!C.mma_step(v_geom(32, HID), id_l, PH_QKV, l)) return;
-    if (warp == 0) {
-      C.read_rows(y);
+    C.stage(l == 0 ? 0 : l - 1, VX_H, HID, L.ln_in, s->hres, c, p.layer_bf16, l == 0, gq.KS, gq.N);
+    if (!C.mma_step(v_geom(128, gq.KS), gq.N, id_q, PH_QKV, l)) return;
+    if (epi) C.read_part(gq.R);
+    bar_consumers(NCT);
+    for (int i = tid; i < gq.R * p.k; i += NCT) {
+      const int r = i % gq.R, t = i / gq.R;
       const int which = c < 64 ? M_Q : (c < 96 ? M_K : M_V);
-      const int mrow = 32 * (c < 64 ? c : (c < 96 ? c - 64 : c - 96)) + lane;
-      const float sc = C.row_scale(L.m[which], mrow);
-      for (int t = 0; t < p.k; ++t)
-        st_relaxed_u32(vx(p, l, t) + VX_QKV + 32 * c + lane, __float_as_uint(y[t] * sc * C.inv_rms(t)));
+      const int mrow = 32 * (c < 64 ? c : (c < 96 ? c - 64 : c - 96)) + r;
+      const float v = C.seg_sum(gq.R, gq.S, r, t) * C.row_scale(L.m[which], mrow) * C.inv_rms(t);
+      st_relaxed_u32(vx(p, l, t) + VX_QKV + 32 * c + r, __float_as_uint(v));
     }
     // ---- attention, one (q head, token) pair per CTA
     if (c < NQH * p.k && !v_attention(C, l)) return;
     // ---- o_proj: rows 8 c .. 8 c + 7, plus the residual
-    C.stage(l, VX_ATT, QROWS, nullptr, nullptr, -1, p.layer_bf16, false);
-    if (!C.mma_step(v_geom(8, QROWS), id_l, PH_O, l)) return;
-    if (warp == 0) {
-      C.read_rows(y);
-      if (lane < 8) {
-        const float sc = C.row_scale(L.m[M_O], 8 * c + lane);
-        for (int t = 0; t < p.k; ++t)
-          st_relaxed_u32(vx(p, l, t) + VX_HA + 8 * c + lane, __float_as_uint(s->hres[t][lane] + y[t] * sc));
-      }
+    C.stage(l, VX_ATT, QROWS, nullptr, nullptr, -1, p.layer_bf16, false, go.KS, go.N);
+    if (!C.mma_step(v_geom(128, go.KS), go.N, id_o, PH_O, l)) return;
+    if (epi) C.read_part(go.R);
+    bar_consumers(NCT);
+    for (int i = tid; i < go.R * p.k; i += NCT) {
+      const int r = i % go.R, t = i / go.R;
+      const float v = s->hres[t][r] + C.seg_sum(go.R, go.S, r, t) * C.row_scale(L.m[M_O], 8 * c + r);
+      st_relaxed_u32(vx(p, l, t) + VX_HA + 8 * c + r, __float_as_uint(v));
     }
-    // ---- gate/up: FFN units 24 c .. 24 c + 23 (accumulator rows 0..23 gate, 24..47 up), SwiGLU
-    C.stage(l, VX_HA, HID, L.ln_post, s->hres2, c, p.layer_bf16, false);
-    if (!C.mma_step(v_geom(48, HID), id_l, PH_GATEUP, l)) return;
-    if (warp < 2) {
-      C.read_rows(y);
-      if (row < 48) {
-        const float sc = C.row_scale(L.m[row < 24 ? M_GATE : M_UP], 24 * c + (row % 24));
-        for (int t = 0; t < p.k; ++t) s->gu[t][row] = y[t] * sc * C.inv_rms(t);
-      }
+    // ---- gate/up (CTAs 0..95): FFN units 32 c .. 32 c + 31 (rows 0..31 gate, 32..63 up), SwiGLU;
+    // every CTA stages (its rows of h_attn are down_proj's residual)
+    C.stage(l, VX_HA, HID, L.ln_post, s->hres2, c, p.layer_bf16, false, gg.KS, gg.N);
+    if (gu_cta) {
+      if (!C.mma_step(v_geom(128, gg.KS), gg.N, id_g, PH_GATEUP, l)) return;
+      if (epi) C.read_part(gg.R);
     }
     bar_consumers(NCT);
-    if (tid < 24) {
-      for (int t = 0; t < p.k; ++t) {
-        const float gt = s->gu[t][tid], up = s->gu[t][24 + tid];
-        st_relaxed_u32(vx(p, l, t) + VX_ACT + 24 * c + tid, __float_as_uint(gt / (1.0f + expf(-gt)) * up));
-      }
+    for (int i = tid; gu_cta && i < gg.R * p.k; i += NCT) {
+      const int r = i % gg.R, t = i / gg.R;
+      const float sc = C.row_scale(L.m[r < 32 ? M_GATE : M_UP], 32 * c + (r % 32));
+      s->gu[t][r] = C.seg_sum(gg.R, gg.S, r, t) * sc * C.inv_rms(t);
+    }
+    bar_consumers(NCT);
+    for (int i = tid; gu_cta && i < 32 * p.k; i += NCT) {
+      const int u = i % 32, t = i / 32;
+      const float gt = s->gu[t][u], up = s->gu[t][32 + u];
+      st_relaxed_u32(vx(p, l, t) + VX_ACT + 32 * c + u, __float_as_uint(gt / (1.0f + expf(-gt)) * up));
     }
     // ---- down_proj: rows 8 c .. 8 c + 7, plus the residual
-    C.stage(l, VX_ACT, FFN, nullptr, nullptr, -1, p.layer_bf16, false);
-    if (!C.mma_step(v_geom(8, FFN), id_l, PH_DOWN, l)) return;
-    if (warp == 0) {
-      C.read_rows(y);
-      if (lane < 8) {
-        const float sc = C.row_scale(L.m[M_DOWN], 8 * c + lane);
-        for (int t = 0; t < p.k; ++t)
-          st_relaxed_u32(vx(p, l, t) + VX_H + 8 * c + lane, __float_as_uint(s->hres2[t][lane] + y[t] * sc));
-      }
+    C.stage(l, VX_ACT, FFN, nullptr, nullptr, -1, p.layer_bf16, false, gd.KS, gd.N);
+    if (!C.mma_step(v_geom(128, gd.KS), gd.N, id_d, PH_DOWN, l)) return;
+    if (epi) C.read_part(gd.R);
+    bar_consumers(NCT);
+    for (int i = tid; i < gd.R * p.k; i += NCT) {
+      const int r = i % gd.R, t = i / gd.R;
+      const float v = s->hres2[t][r] + C.seg_sum(gd.R, gd.S, r, t) * C.row_scale(L.m[M_DOWN], 8 * c + r);
+      st_relaxed_u32(vx(p, l, t) + VX_H + 8 * c + r, __float_as_uint(v));
     }
   }
   // ---- final RMSNorm + LM head in chunks of 128 rows, one running argmax per token
-  C.stage(p.n_layers - 1, VX_H, HID, p.final_norm, nullptr, -1, p.head_bf16, false);
+  C.stage(p.n_layers - 1, VX_H, HID, p.final_norm, nullptr, -1, p.head_bf16, false, HID, VN);
   float best[VK];
   int besti[VK];
 #pragma unroll
@@ -688,9 +727,9 @@ __device__ void v_run(VCons& C) {
   const int v0 = (int)((long long)p.vocab * c / V_GRID), v1 = (int)((long long)p.vocab * (c + 1) / V_GRID);
   for (int q = 0; v0 + V_HEAD_CHUNK * q < v1; ++q) {
     const int r0 = v0 + V_HEAD_CHUNK * q, nr = min(V_HEAD_CHUNK, v1 - r0);
-    if (!C.mma_step(v_geom((nr + 7) & ~7, HID), id_h, PH_HEAD, p.n_layers)) return;
+    if (!C.mma_step(v_geom((nr + 7) & ~7, HID), VN, id_h, PH_HEAD, p.n_layers)) return;
     if (epi) {
-      C.read_rows(y);
+      C.read_seg(128, y);
       if (row < nr) {
         const int r = r0 + row;
         const float sc = C.row_scale(p.embed, r);

@@ -15,28 +15,53 @@ namespace mk {
 constexpr uint32_t X_EMPTY = 0xFFFFFFFFu;
 
 constexpr int VK = 8;        // tokens per verify launch, at most
-constexpr int VN = 16;       // MMA N: B rows 0..7 hold the tokens' high parts, rows 8..15 the low parts
+constexpr int VN = 16;       // B rows a segment: 0..7 the tokens' high parts, 8..15 the low parts
 constexpr int V_NSLOT = 6;   // weight ring slots (SLOT bytes each)
 constexpr int V_GRID = 128;  // the verify grid (one CTA per SM)
 constexpr int V_HEAD_CHUNK = 128;  // LM-head rows per MMA (M = 128)
 constexpr int V_MAXPOS = 1024;     // positions a verify step attends over, at most (pos0 + k)
 
-// The GEMM steps of a layer and their per-CTA operand blocks. Each CTA's rows of a step are stored
-// as 16-bit values in "boxes" of 64 input columns: box j holds R8 rows (the CTA's rows rounded up to
-// a multiple of 8, zero-padded) x 128 bytes, 128-byte swizzled, so one bulk copy puts a run of boxes
-// into shared memory in the layout the MMA reads. Boxes of a block are contiguous.
+// The GEMM steps of a layer and their per-CTA operand blocks. A CTA owns R whole rows of a step
+// (all K inputs of each), split into S segments of KS = K / S inputs; its block is stored as
+// 128-row tiles ("boxes") of 64 input columns, 16-bit values, 128-byte swizzled, where tile row
+// L = seg * R + r holds row r's inputs seg * KS + 64 b .. + 63 (box b of KS / 64). S * R = 128, so
+// every row of every MMA is a real weight row; the B operand holds, for segment seg, the k token
+// vectors' inputs of that segment (rows 16 seg + t: high parts, 16 seg + 8 + t: low parts), so the
+// diagonal blocks D[seg * R + r][16 seg + ...] of the product are row r's partial sums, which the
+// epilogue adds in segment order. One box fills one ring slot (16 KB).
 enum VStep { VS_QKV = 0, VS_O = 1, VS_GU = 2, VS_DOWN = 3, VS_COUNT = 4 };
-__host__ __device__ inline int v_rows8(int step) { return step == VS_QKV ? 32 : (step == VS_GU ? 48 : 8); }
-__host__ __device__ inline int v_cols(int step) { return step == VS_O ? QROWS : (step == VS_DOWN ? FFN : HID); }
-__host__ __device__ inline size_t v_block_bytes(int step) { return (size_t)v_rows8(step) * v_cols(step) * 2; }
-// Bytes of one layer's blocks (all steps, all CTAs) and the offset of step s's blocks in a layer.
-__host__ __device__ inline size_t v_layer_bytes() {
-  return (size_t)V_GRID * (v_block_bytes(0) + v_block_bytes(1) + v_block_bytes(2) + v_block_bytes(3));
+constexpr int V_GU_CTAS = 96;  // gate/up: CTAs 0..95 own 32 FFN units (32 gate + 32 up rows) each
+struct VStepGeom {
+  int R, S, KS, KB, N;  // rows, segments, inputs a segment, boxes (KS / 64), MMA N (16 S)
+};
+__host__ __device__ inline VStepGeom v_step_geom(int step) {
+  switch (step) {
+    case VS_QKV: return {32, 4, 256, 4, 64};
+    case VS_O: return {8, 16, 128, 2, 256};
+    case VS_GU: return {64, 2, 512, 8, 32};
+    default: return {8, 16, 192, 3, 256};
+  }
 }
-__host__ __device__ inline size_t v_step_offset(int s) {
+__host__ __device__ inline int v_cols(int step) { return step == VS_O ? QROWS : (step == VS_DOWN ? FFN : HID); }
+// Boxes of CTA c's block of a step (gate/up: none for CTAs V_GU_CTAS..).
+__host__ __device__ inline int v_nbox(int step, int c) {
+  return (step == VS_GU && c >= V_GU_CTAS) ? 0 : v_step_geom(step).KB;
+}
+constexpr size_t V_BOX = 16384;  // 128 rows x 64 columns x 2 bytes
+// Bytes of one layer's blocks (all steps, all CTAs); steps are stored one after another, each as
+// its CTAs' blocks in CTA order.
+__host__ __device__ inline size_t v_step_bytes(int step) {
+  const int ctas = step == VS_GU ? V_GU_CTAS : V_GRID;
+  return (size_t)ctas * v_step_geom(step).KB * V_BOX;
+}
+__host__ __device__ inline size_t v_layer_bytes() {
+  return v_step_bytes(VS_QKV) + v_step_bytes(VS_O) + v_step_bytes(VS_GU) + v_step_bytes(VS_DOWN);
+}
+// Offset of CTA c's block of step s within a layer.
+__host__ __device__ inline size_t v_block_offset(int s, int c) {
   size_t o = 0;
-  for (int i = 0; i < s; ++i) o += (size_t)V_GRID * v_block_bytes(i);
-  return o;
+  for (int i = 0; i < s; ++i) o += v_step_bytes(i);
+  return o + (size_t)c * v_step_geom(s).KB * V_BOX;
 }
 // LM head: CTA c's rows split_range(vocab, V_GRID, c) in chunks of V_HEAD_CHUNK rows; every chunk
 // gets a full V_HEAD_CHUNK x HID block (the last one zero-padded).
