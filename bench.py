@@ -18,7 +18,8 @@ returns each token to the host), `clocks` (NVML samples during the timed region)
 `stream_read_gbs` (the library's bulk-copy streaming-read probe, same run), `variants` (the FP8,
 NVFP4 (amax and searched block scales; all-NVFP4), bf16-head FP8, bf16-scale FP8 and long-context
 FP8 workloads, each timed the same way), `xray` (the instrumented build's split of a token, its
-overhead and its span against the launch time, for the headline and the long-context workload),
+overhead against the plain build over the same positions and its span against the launch time,
+for the headline and the long-context workload),
 `layer1_bf16` (one layer + the LM head, timed cold after an L2 scrub and warm) and `sweep`
 (throughput and energy against context length, FP8).
 
@@ -336,30 +337,44 @@ def run_cpu_leg(wl: S.Workload, seconds: float, one_thread_seconds: float):
     print(json.dumps(allc))
 
 
-def xray_summary(wl: S.Workload, mk, master, steps: int = 16, plain_tok_s: float | None = None):
-    """The same workload through the instrumented build (MK_FLAG_XRAY): the last step's split of a
-    token into weight-read, wait, attention and LM-head time, the instrumented throughput against
-    the plain one, and the X-ray's own span of the last step against that launch's CUDA-event time
-    (the two checks of the X-ray milestone: overhead within 3 %, summed phases within 5 %)."""
+def xray_summary(wl: S.Workload, mk, master, steps: int = 64, runs: int = 3):
+    """The workload through the instrumented build (MK_FLAG_XRAY): the last step's split of a token
+    into weight-read, wait, attention and LM-head time, the critical path per layer, and the X-ray
+    milestone's two checks: instrumented throughput against the plain build's over the same
+    positions (plain and instrumented regions alternate, `runs` each; medians) and the first-to-last
+    stamp span of the last step against that launch's CUDA-event time."""
     from quantized_gemv_gb300 import xray
-    cfg, _, model, pos0, first = setup_model(wl, mk, flags=mk.MK_FLAG_XRAY, master=master)
-    total_ms, per, _ = time_steps(model, first, pos0, steps, 3)
-    tr = model.trace()
+    cfg, master, plain, pos0, first = setup_model(wl, mk, master=master)
+    _, _, inst, _, _ = setup_model(wl, mk, flags=mk.MK_FLAG_XRAY, master=master)
+    k = min(steps, cfg.max_ctx - pos0)
+
+    def rate(model):
+        t_ms, per, _ = time_steps(model, first, pos0, k, 3)
+        return k / (t_ms * 1e-3), per
+
+    rp, ri = [], []
+    for _ in range(runs):
+        rp.append(rate(plain)[0])
+        r, per = rate(inst)
+        ri.append(r)
+    tr = inst.trace()  # the last instrumented step
     a = xray.analyze(tr)
     cp = xray.critical_path(tr)
-    model.close()
+    plain.close()
+    inst.close()
     t = a["token_ns"]
-    inst = steps / (total_ms * 1e-3)
+    p_med, i_med = float(np.median(rp)), float(np.median(ri))
     return {"token_us": round(t / 1e3, 1), "ctas": a["ctas"],
             "weight_read_share": round(a["weight_read_ns"] / t, 3), "barrier_wait_share": round(a["barrier_wait_share"], 3),
             "attention_share": round(a["attention_ns"] / t, 3), "lm_head_share": round(a["lm_head_ns"] / t, 3),
-            "instrumented_tok_s": round(inst, 1),
-            "overhead_vs_plain": round(plain_tok_s / inst - 1.0, 4) if plain_tok_s else None,
+            "plain_tok_s": round(p_med, 1), "instrumented_tok_s": round(i_med, 1),
+            "overhead_vs_plain": round(p_med / i_med - 1.0, 4),
             "last_launch_us": round(per[-1] * 1e3, 1),
             "span_over_launch": round(t / 1e3 / (per[-1] * 1e3), 4),
-            "critical_path_us": {k: round(v / 1e3, 3) for k, v in cp.items() if k != "layers"},
-            "note": f"the last of {steps} instrumented steps from position {pos0}; shares of the token's wall "
-                    "time, averaged over CTAs; span_over_launch = first-to-last stamp / CUDA-event launch time"}
+            "critical_path_us": {kk: round(v / 1e3, 3) for kk, v in cp.items() if kk != "layers"},
+            "note": f"{runs} alternating regions of {k} steps from position {pos0} per build (medians); the split "
+                    "is the last instrumented step's, shares of the token's wall time averaged over CTAs; "
+                    "span_over_launch = first-to-last stamp / CUDA-event launch time"}
 
 
 SWEEP_POSITIONS = (16, 128, 512, 1024, 2048)
@@ -599,11 +614,10 @@ def main():
                               "e2e_tok_s": round(r2["e2e_tok_s"], 1), "clocks": r2["clocks"]}
     xr = None
     if rank == 0 and not args.no_xray:
-        xr = xray_summary(wl, mk, master, plain_tok_s=res["runs"]["median_tok_s"])
+        xr = xray_summary(wl, mk, master, steps=min(args.steps, wl.steps))
         if not args.no_variants and wl.name != "qwen3_0.6b_fp8_ctx4096":
-            v = variants.get("qwen3_0.6b_fp8_ctx4096")
-            xr_ctx = xray_summary(S.WORKLOADS["qwen3_0.6b_fp8_ctx4096"], mk, None,
-                                  plain_tok_s=v["runs"]["median_tok_s"] if v else None)
+            w4 = S.WORKLOADS["qwen3_0.6b_fp8_ctx4096"]
+            xr_ctx = xray_summary(w4, mk, None, steps=min(args.steps, w4.steps))
             xr = {"headline": xr, "qwen3_0.6b_fp8_ctx4096": xr_ctx}
     layer1 = run_layer1(mk) if rank == 0 and not args.no_layer1 else None
     verify = (run_verify(mk, wl.name if wl.prefill + wl.prompt_len + 8 * 19 <= 1024 else HEADLINE)

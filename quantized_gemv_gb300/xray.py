@@ -27,9 +27,11 @@ def records(trace: np.ndarray):
     """Yield (cta, [(t_ns, phase, kind), ...]) for every CTA that wrote records (phase and wait
     stamps; sub-phase marks, which carry only the SM clock, are left out).
 
-    Begin stamps (phase and wait begins) carry only the SM clock (their %globaltimer field is 0):
-    their global time is interpolated linearly in clock64 between the CTA's neighbouring stamps
-    that carry both, which is exact while the SM clock holds still between them."""
+    Most stamps carry only the SM clock (their %globaltimer field is 0; the kernel reads the global
+    timer only at the embedding, at the start of each layer's wait for the previous layer's output
+    and at the end of the LM head): their global time is interpolated linearly in clock64 between
+    the CTA's neighbouring stamps that carry both, which is exact while the SM clock holds still
+    between them."""
     for cta in range(trace.shape[0]):
         rows = trace[cta]
         ends = np.flatnonzero((rows["kind"] == KIND_STOP) | ((rows["gtime"] == 0) & (rows["clk"] == 0)))

@@ -13,12 +13,14 @@ QKV, ATT, O, GU, DOWN, HEAD, EMBED = 0, 1, 2, 3, 4, 5, 6
 
 
 def _trace(rows_per_cta, width=64, clock_only_begins=False):
-    """Records {t, clk = 7 t + 1}; with clock_only_begins, phase and wait begins keep only the
-    clock (gtime 0), as the kernel writes them after the embedding's first stamp."""
+    """Records {t, clk = 7 t + 1}; with clock_only_begins, only the embedding's stamps, the start of
+    each wait on the down phase and the LM head's end keep the global time (the others gtime 0), as
+    the kernel writes them."""
     tr = np.zeros((len(rows_per_cta), width), dtype=TRACE_DTYPE)
     for c, rows in enumerate(rows_per_cta):
         for i, (t, ph, kind) in enumerate(rows + [(0, 0, STOP)]):
-            g = 0 if (clock_only_begins and kind in (B, WB) and ph != EMBED) else t
+            anchor = ph == EMBED or (ph == HEAD and kind == E) or (ph == DOWN and kind == WB)
+            g = 0 if (clock_only_begins and kind != MARK and not anchor) else t
             tr[c][i] = (g, 7 * t + 1, 3, c, ph, kind)
     return tr
 
@@ -192,7 +194,15 @@ def test_stamps_only_build_has_no_marks_and_spans_the_launch():
     for c in range(tr.shape[0]):
         stop = np.flatnonzero(tr[c]["kind"] == STOP)
         kinds |= set(np.unique(tr[c][: stop[0]]["kind"]).tolist())
-    assert MARK not in kinds
+    assert kinds <= {B, E, WB, WE}  # no sub-phase marks
+    for cta, recs in xray.records(tr):  # every CTA's stamps reached the trace, in order
+        begins = [ph for _, ph, k in recs if k == B]
+        for ph in (QKV, GU, DOWN):
+            assert begins.count(ph) == cfg.n_layers, (cta, ph)
+        assert begins.count(HEAD) == 1
+        ts = [t for t, _, _ in recs]
+        assert ts == sorted(ts)
     span = xray.analyze(tr)["token_ns"]
     assert 0.95 * launch_ns <= span <= launch_ns, (span, launch_ns)
     xr.close()
+
