@@ -107,3 +107,35 @@ def test_verify_full_bf16_model(k):
     _, matches = _verify_against_oracle(model, om, toks, wl.prompt_len, k)
     assert matches >= k - 1
     model.close()
+
+
+@pytest.mark.parametrize("variant", ["fp8", "nvfp4"])
+def test_verify_full_quantised_model(variant):
+    """The 28-layer FP8 and NVFP4 models (their tiles held as f16, the codes exact) after the 32-token
+    prompt, k = 8: the tokens and logits of eight teacher-forced oracle steps."""
+    wl = S.WORKLOADS["qwen3_0.6b_" + variant]
+    cfg = wl.config()
+    _, model, om = make_pair(cfg, variant, seed=0)
+    model.verify_attach()
+    prompt = S.prompt_ids(cfg, wl.prompt_len)
+    toks = np.concatenate([prompt, S.prompt_ids(cfg, 8, seed=19)])
+    _prefix(model, om, toks, wl.prompt_len)
+    _, matches = _verify_against_oracle(model, om, toks, wl.prompt_len, 8)
+    assert matches >= 7
+    model.close()
+
+
+def test_verify_at_the_position_limit():
+    """pos0 = 1016, k = 8: the last token attends over all 1,024 positions the verify step allows
+    (1,016 of them prefilled in both caches), so every score slot is used; one position further is
+    rejected."""
+    cfg = S.ModelConfig(n_layers=2, vocab=4099, max_ctx=1100)
+    _, model, om = make_pair(cfg, "bf16", seed=151, prefill=1016)
+    model.verify_attach()
+    toks = S.prompt_ids(cfg, 1024, seed=51)
+    _, matches = _verify_against_oracle(model, om, toks, 1016, 8)
+    assert matches >= 7
+    nxt = torch.zeros(8, dtype=torch.int32, device="cuda")
+    with pytest.raises(mk.MkError):
+        model.verify_step(torch.zeros(8, dtype=torch.int32, device="cuda"), 1017, nxt)
+    model.close()
