@@ -127,12 +127,12 @@ constexpr int V_XB = v_xb_bytes(3, 256);
 static_assert(v_xb_bytes(4, 64) <= V_XB && v_xb_bytes(2, 256) <= V_XB && v_xb_bytes(8, 32) <= V_XB &&
                   v_xb_bytes(HID / 64, VN) <= V_XB,
               "a step's B operand exceeds the staging buffer");
-constexpr uint32_t V_TMEM_COLS = 256;  // D: 128 lanes x N (<= 256) fp32 columns
+constexpr uint32_t V_TMEM_COLS = 512;  // two accumulators of 128 lanes x N (<= 256) fp32 columns
 
 struct __align__(16) VSmem {
   uint64_t full[V_NSLOT];
   uint64_t empty[V_NSLOT];  // arrived by tcgen05.commit when the MMAs reading the slot completed
-  uint64_t done;            // arrived by tcgen05.commit when a step's MMAs completed
+  uint64_t done;            // arrived by both issuers' tcgen05.commit when a step's MMAs completed
   uint32_t tmem;            // tensor memory base address
   volatile int flag;         // stays 0: the wait for the MMAs' completion after an abort
   volatile int abort;
@@ -272,8 +272,9 @@ struct VCons {
   uint8_t* ring;
   uint8_t* xb;
   int tid, lane, warp;
-  uint32_t n;      // ring slots consumed (the MMA issuer's count)
+  uint32_t n;      // ring slots consumed
   uint32_t ndone;  // GEMM steps completed (parity of `done`)
+  bool acc2;       // the last GEMM step used the second accumulator
 
   // Stage the k input vectors of a GEMM step into the B operand of a step with segments of KS inputs
   // and N rows: input e of token t, in segment seg = e / KS, goes to box (e % KS) / 64, high part in
@@ -402,40 +403,50 @@ struct VCons {
   }
 
   // The MMAs of one GEMM step: D[row][n] = sum over the step's boxes of A (ring slots) x B (xb, boxes
-  // of N rows), one accumulator. Thread 0 issues them slot by slot, each slot committed to its
-  // empty barrier, and finally commits `done`; every thread then waits for `done`. Returns false
-  // after an abort.
+  // of N rows). One thread issuing MMAs sets the pace (each costs it tens of cycles whatever its
+  // size), so two issue them: thread 0 the even ring slots of the step into accumulator 0 (tensor
+  // memory columns 0 .. N - 1), thread 32 the odd ones into accumulator 1 (columns N .. 2N - 1).
+  // Each commits its slots to their empty barriers, so a slot is refilled as soon as the tensor
+  // core has read it, and finally commits `done` (two arrivals); every thread then waits for it.
+  // The epilogue adds the two accumulators (read_seg). Returns false after an abort.
   __device__ bool mma_step(VGeom g, int N, uint32_t idesc, int phase, int layer) {
     const VParams& p = *P;
+    const int nslots = g.slots();
+    acc2 = nslots > 1;
     bar_consumers(NCT);  // the staged operand and the previous step's tensor-memory reads
-    if (tid == 0) {
+    if (tid == 0 || tid == 32) {
+      const int who = tid >> 5;
       tc_fence_after();
-      int j = 0;
-      const uint32_t xbase = smem_u32(xb);
-      for (int sl = 0; sl < g.slots(); ++sl, ++n) {
-        const uint32_t slot = n % V_NSLOT, par = (n / V_NSLOT) & 1;
+      const uint32_t xbase = smem_u32(xb), d = s->tmem + (uint32_t)(who * N);
+      bool first = true;
+      for (int sl = who; sl < nslots; sl += 2) {
+        const uint32_t m = n + (uint32_t)sl, slot = m % V_NSLOT, par = (m / V_NSLOT) & 1;
         if (s->abort) break;
         if (!v_wait(&s->full[slot], par, &s->abort, p.timeout_ns)) {
           if (!s->abort) v_fail(p, s, 3u, (uint32_t)(phase | (layer << 8) | (blockIdx.x << 16)) | 0x80000000u);
           break;
         }
         const uint32_t sbase = smem_u32(ring + (size_t)slot * SLOT);
+        const int j0 = sl * g.bps;  // the slot's first box
         // the MMA reads 128 rows (16 KB) from a box's start, which end inside the ring and xb, and
         // N rows of each B box
         if (!mk_in_bounds(slot < V_NSLOT && (slot + 1) * SLOT + (g.bps - 1) * g.R8 * 128 <= V_RING + V_XB - 16384 + SLOT &&
-                              (min(g.nbox, j + g.bps)) * N * 128 <= V_XB,
+                              (min(g.nbox, j0 + g.bps)) * N * 128 <= V_XB,
                           p.sync->status, 14, slot))
           break;
-        for (int b = 0; b < g.bps && j < g.nbox; ++b, ++j) {
+        for (int b = 0, j = j0; b < g.bps && j < g.nbox; ++b, ++j) {
 #pragma unroll
-          for (int kk = 0; kk < 4; ++kk)
-            umma_f16(s->tmem, umma_desc_sw128(sbase + (uint32_t)(b * g.R8 * 128 + 32 * kk)),
-                     umma_desc_sw128(xbase + (uint32_t)(j * N * 128 + 32 * kk)), idesc, (j > 0 || kk != 0) ? 1u : 0u);
+          for (int kk = 0; kk < 4; ++kk) {
+            umma_f16(d, umma_desc_sw128(sbase + (uint32_t)(b * g.R8 * 128 + 32 * kk)),
+                     umma_desc_sw128(xbase + (uint32_t)(j * N * 128 + 32 * kk)), idesc, first ? 0u : 1u);
+            first = false;
+          }
         }
         umma_commit(&s->empty[slot]);
       }
       umma_commit(&s->done);  // also after an abort: the issued MMAs finish before the CTA exits
     }
+    n += (uint32_t)nslots;
     // every thread waits for the MMAs (they were committed even after an abort, so they end first)
     const bool ok = v_wait(&s->done, ndone & 1, &s->abort, p.timeout_ns) || v_wait(&s->done, ndone & 1, &s->flag, p.timeout_ns);
     ++ndone;
@@ -445,31 +456,41 @@ struct VCons {
     return s->abort == 0;
   }
   // This thread's accumulator row (warps 0..3: tensor-memory lane L = 32 warp + lane, tile row
-  // seg * R + r with seg = L / R) on its own segment's diagonal block: y[t] = D[L][16 seg + t] +
+  // seg * R + r with seg = L / R) on its own segment's diagonal block, both accumulators added
+  // (the second only where the step had more than one ring slot): y[t] = D[L][16 seg + t] +
   // D[L][16 seg + 8 + t] (high and low parts). A warp's lanes may lie in several segments (R < 32):
   // the warp loads each of their column blocks and every lane keeps its own.
-  __device__ void read_seg(int R, float* y) {
+  __device__ void read_seg(int R, int N, float* y) {
     const int L = 32 * warp + lane, seg = L / R;
     const int s0 = (32 * warp) / R, s1 = (32 * warp + 31) / R;
-    float d[16];
+    const uint32_t base = s->tmem + ((uint32_t)(32 * warp) << 16);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) d[i] = 0.f;
-    for (int sg = s0; sg <= s1; ++sg) {  // warp-uniform
-      float v[16];
-      tmem_ld16(s->tmem + ((uint32_t)(32 * warp) << 16) + (uint32_t)(VN * sg), v);
+    for (int t = 0; t < VK; ++t) y[t] = 0.f;
+    for (int sg = s0; sg <= s1; ++sg) {  // warp-uniform; per token: hi0 + lo0, then + hi1, + lo1
+      float h[8], a[8];
+      tmem_ld8(base + (uint32_t)(VN * sg), h);
+      tmem_ld8(base + (uint32_t)(VN * sg + 8), a);
+#pragma unroll
+      for (int t = 0; t < 8; ++t) h[t] += a[t];
+      if (acc2) {
+        tmem_ld8(base + (uint32_t)(N + VN * sg), a);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) h[t] += a[t];
+        tmem_ld8(base + (uint32_t)(N + VN * sg + 8), a);
+#pragma unroll
+        for (int t = 0; t < 8; ++t) h[t] += a[t];
+      }
       if (sg == seg) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) d[i] = v[i];
+        for (int t = 0; t < VK; ++t) y[t] = h[t];
       }
     }
-#pragma unroll
-    for (int t = 0; t < VK; ++t) y[t] = d[t] + d[8 + t];
     tc_fence_before();
   }
   // Warps 0..3: this thread's diagonal-block row into part[L] (see read_seg).
-  __device__ void read_part(int R) {
+  __device__ void read_part(int R, int N) {
     float y[VK];
-    read_seg(R, y);
+    read_seg(R, N, y);
 #pragma unroll
     for (int t = 0; t < VK; ++t) s->part[32 * warp + lane][t] = y[t];
   }
@@ -667,7 +688,7 @@ __device__ void v_run(VCons& C) {
     // ---- q|k|v: this CTA's 32 rows (CTA c writes q|k|v elements 32 c .. 32 c + 31)
     C.stage(l == 0 ? 0 : l - 1, VX_H, HID, L.ln_in, s->hres, c, p.layer_bf16, l == 0, gq.KS, gq.N);
     if (!C.mma_step(v_geom(128, gq.KS), gq.N, id_q, PH_QKV, l)) return;
-    if (epi) C.read_part(gq.R);
+    if (epi) C.read_part(gq.R, gq.N);
     bar_consumers(NCT);
     for (int i = tid; i < gq.R * p.k; i += NCT) {
       const int r = i % gq.R, t = i / gq.R;
@@ -681,7 +702,7 @@ __device__ void v_run(VCons& C) {
     // ---- o_proj: rows 8 c .. 8 c + 7, plus the residual
     C.stage(l, VX_ATT, QROWS, nullptr, nullptr, -1, p.layer_bf16, false, go.KS, go.N);
     if (!C.mma_step(v_geom(128, go.KS), go.N, id_o, PH_O, l)) return;
-    if (epi) C.read_part(go.R);
+    if (epi) C.read_part(go.R, go.N);
     bar_consumers(NCT);
     for (int i = tid; i < go.R * p.k; i += NCT) {
       const int r = i % go.R, t = i / go.R;
@@ -693,7 +714,7 @@ __device__ void v_run(VCons& C) {
     C.stage(l, VX_HA, HID, L.ln_post, s->hres2, c, p.layer_bf16, false, gg.KS, gg.N);
     if (gu_cta) {
       if (!C.mma_step(v_geom(128, gg.KS), gg.N, id_g, PH_GATEUP, l)) return;
-      if (epi) C.read_part(gg.R);
+      if (epi) C.read_part(gg.R, gg.N);
     }
     bar_consumers(NCT);
     for (int i = tid; gu_cta && i < gg.R * p.k; i += NCT) {
@@ -710,7 +731,7 @@ __device__ void v_run(VCons& C) {
     // ---- down_proj: rows 8 c .. 8 c + 7, plus the residual
     C.stage(l, VX_ACT, FFN, nullptr, nullptr, -1, p.layer_bf16, false, gd.KS, gd.N);
     if (!C.mma_step(v_geom(128, gd.KS), gd.N, id_d, PH_DOWN, l)) return;
-    if (epi) C.read_part(gd.R);
+    if (epi) C.read_part(gd.R, gd.N);
     bar_consumers(NCT);
     for (int i = tid; i < gd.R * p.k; i += NCT) {
       const int r = i % gd.R, t = i / gd.R;
@@ -729,7 +750,7 @@ __device__ void v_run(VCons& C) {
     const int r0 = v0 + V_HEAD_CHUNK * q, nr = min(V_HEAD_CHUNK, v1 - r0);
     if (!C.mma_step(v_geom((nr + 7) & ~7, HID), VN, id_h, PH_HEAD, p.n_layers)) return;
     if (epi) {
-      C.read_seg(128, y);
+      C.read_seg(128, VN, y);
       if (row < nr) {
         const int r = r0 + row;
         const float sc = C.row_scale(p.embed, r);
@@ -795,7 +816,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) k_verify(const VParams p) {
       mbar_init(&s->full[i], 1);
       mbar_init(&s->empty[i], 1);
     }
-    mbar_init(&s->done, 1);
+    mbar_init(&s->done, 2);  // one arrival per MMA issuer
     s->abort = 0;
     s->flag = 0;
     fence_mbar_init();
