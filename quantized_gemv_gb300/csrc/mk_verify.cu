@@ -254,15 +254,21 @@ __device__ void v_producer(const VParams& p, VSmem* s, uint8_t* ring) {
 
 // ------------------------------------------------------------------ consumers
 // 16-bit high and low parts of x (bf16 or f16): x - hi is exact in fp32 and lo rounds it.
-__device__ __forceinline__ void v_split(float x, int ab_bf16, uint16_t& hi, uint16_t& lo) {
+// Two elements at once (packed conversions, the same roundings): hw and lw hold the high and low
+// parts of a in their low halves and of b in their high halves.
+__device__ __forceinline__ void v_split2(float a, float b, int ab_bf16, uint32_t& hw, uint32_t& lw) {
   if (ab_bf16) {
-    const __nv_bfloat16 h = __float2bfloat16_rn(x);
-    hi = __bfloat16_as_ushort(h);
-    lo = __bfloat16_as_ushort(__float2bfloat16_rn(x - __bfloat162float(h)));
+    const __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+    const float2 hf = __bfloat1622float2(h);
+    const __nv_bfloat162 l = __floats2bfloat162_rn(a - hf.x, b - hf.y);
+    hw = *reinterpret_cast<const uint32_t*>(&h);
+    lw = *reinterpret_cast<const uint32_t*>(&l);
   } else {
-    const __half h = __float2half_rn(x);
-    hi = __half_as_ushort(h);
-    lo = __half_as_ushort(__float2half_rn(x - __half2float(h)));
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - hf.x, b - hf.y);
+    hw = *reinterpret_cast<const uint32_t*>(&h);
+    lw = *reinterpret_cast<const uint32_t*>(&l);
   }
 }
 
@@ -364,21 +370,18 @@ struct VCons {
             for (int e = 0; e < 8; ++e) res[t][e] = v[e];
           }
           float ss = 0.f;
-          uint16_t hi[8], lo[8];
+          if (w) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            float x = v[e];
-            if (w) {
-              ss = fmaf(x, x, ss);
-              x *= __uint_as_float((uint32_t)__ldg(w + e0 + e) << 16);
+            for (int e = 0; e < 8; ++e) {
+              ss = fmaf(v[e], v[e], ss);
+              v[e] *= __uint_as_float((uint32_t)__ldg(w + e0 + e) << 16);
             }
-            v_split(x, ab_bf16, hi[e], lo[e]);
           }
           uint4 H, L;
-          H.x = hi[0] | ((uint32_t)hi[1] << 16), H.y = hi[2] | ((uint32_t)hi[3] << 16);
-          H.z = hi[4] | ((uint32_t)hi[5] << 16), H.w = hi[6] | ((uint32_t)hi[7] << 16);
-          L.x = lo[0] | ((uint32_t)lo[1] << 16), L.y = lo[2] | ((uint32_t)lo[3] << 16);
-          L.z = lo[4] | ((uint32_t)lo[5] << 16), L.w = lo[6] | ((uint32_t)lo[7] << 16);
+          v_split2(v[0], v[1], ab_bf16, H.x, L.x);
+          v_split2(v[2], v[3], ab_bf16, H.y, L.y);
+          v_split2(v[4], v[5], ab_bf16, H.z, L.z);
+          v_split2(v[6], v[7], ab_bf16, H.w, L.w);
           const int seg = e0 / KS, j = e0 - seg * KS, n0 = VN * seg;
           uint8_t* box = xb + (size_t)(j / 64) * (N * 128);
           if (mk_in_bounds((j / 64 + 1) * N * 128 <= V_XB && n0 + VN <= N && t < VK, p.sync->status, 11,
