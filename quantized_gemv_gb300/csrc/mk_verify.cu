@@ -470,18 +470,25 @@ struct VCons {
 #pragma unroll
     for (int t = 0; t < VK; ++t) y[t] = 0.f;
     for (int sg = s0; sg <= s1; ++sg) {  // warp-uniform; per token: hi0 + lo0, then + hi1, + lo1
-      float h[8], a[8];
-      tmem_ld8(base + (uint32_t)(VN * sg), h);
-      tmem_ld8(base + (uint32_t)(VN * sg + 8), a);
-#pragma unroll
-      for (int t = 0; t < 8; ++t) h[t] += a[t];
+      uint32_t r0[8], r1[8], r2[8], r3[8];
+      tmem_ld8_issue(base + (uint32_t)(VN * sg), r0);  // the segment's loads in flight together
+      tmem_ld8_issue(base + (uint32_t)(VN * sg + 8), r1);
       if (acc2) {
-        tmem_ld8(base + (uint32_t)(N + VN * sg), a);
+        tmem_ld8_issue(base + (uint32_t)(N + VN * sg), r2);
+        tmem_ld8_issue(base + (uint32_t)(N + VN * sg + 8), r3);
+      }
+      tmem_wait_ld8(r0);
+      tmem_wait_ld8(r1);
+      if (acc2) {
+        tmem_wait_ld8(r2);
+        tmem_wait_ld8(r3);
+      }
+      float h[8];
 #pragma unroll
-        for (int t = 0; t < 8; ++t) h[t] += a[t];
-        tmem_ld8(base + (uint32_t)(N + VN * sg + 8), a);
+      for (int t = 0; t < 8; ++t) h[t] = __uint_as_float(r0[t]) + __uint_as_float(r1[t]);
+      if (acc2) {
 #pragma unroll
-        for (int t = 0; t < 8; ++t) h[t] += a[t];
+        for (int t = 0; t < 8; ++t) h[t] = (h[t] + __uint_as_float(r2[t])) + __uint_as_float(r3[t]);
       }
       if (sg == seg) {
 #pragma unroll
